@@ -1,0 +1,264 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle.
+
+Route packing must be bit-exact; layer outputs within relative L2 2e-3 and
+max-abs 1e-2 of the oracle; a row's bytes identical across batch sizes,
+chunk splits, member counts and capacities (TensorFold #837, "Receipt";
+exllamav3 #284, "Validation")."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import trellis_quantized_moe_gb300 as X  # noqa: E402
+from oracle import exl3_oracle as O  # noqa: E402
+from workloads import (CB_3INST, CB_MCG, CB_MUL1, LinearWorkload, MoEWorkload,  # noqa: E402
+                       act_to_f64, config)
+from gpu_common import (assert_close, moe_inputs, oracle_rows, out_tensor, to_device,  # noqa: E402
+                        to_f64)
+
+
+# --------------------------------------------------------------------------- route pack
+def _pack_on_gpu(ids_np, E, cap, dtype):
+    ids = torch.from_numpy(ids_np.astype(np.int64 if dtype == "i64" else np.int32)).cuda()
+    M, topk = ids_np.shape
+    R = M * topk
+    nt = X.exl3_route_pack_max_tiles(M, topk, E, cap)
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    packed = torch.full((max(R, 1),), -7, dtype=torch.int32, device="cuda")
+    tiles = torch.full((max(nt, 1), 3), -7, dtype=torch.int32, device="cuda")
+    info = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    X.exl3_route_pack(ids, E, cap, off, packed, tiles, info)
+    torch.cuda.synchronize()
+    info = info.cpu().numpy()
+    return (off.cpu().numpy(), packed.cpu().numpy()[:R], tiles.cpu().numpy()[:info[1]], info)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_route_pack_bit_exact_on_configs(cfg):
+    s = config(cfg, M={1: 128}.get(cfg))
+    w = MoEWorkload(s)
+    off, packed, tiles, info = _pack_on_gpu(w.ids, s.E, s.capacity, s.ids_dtype)
+    r_off, r_packed, r_tiles, r_nact = O.route_pack(w.ids, s.E, s.capacity)
+    assert info[0] == 0
+    assert np.array_equal(off, r_off) and np.array_equal(packed, r_packed)
+    assert np.array_equal(tiles, r_tiles) and info[2] == r_nact
+
+
+@pytest.mark.parametrize("M,topk,E,cap,dt", [
+    (16, 2, 8, 32, "i32"),          # topk=2, capacity = rows
+    (9, 4, 3, 11, "i64"),           # one expert gets exactly capacity + 1
+    (300, 8, 5, 64, "i32"),         # multi-tile spans, multi-step warps
+    (4000, 8, 1000, 7, "i64"),      # many experts, many warps
+    (1, 1, 1, 1, "i32"),
+    (0, 8, 16, 4, "i32"),           # empty batch
+])
+def test_route_pack_edge_cases(M, topk, E, cap, dt):
+    rng = np.random.default_rng(M + E)
+    ids = rng.integers(0, E, size=(M, topk))
+    if M == 9:
+        ids[:, :] = np.arange(M * topk).reshape(M, topk) % 3
+        ids[ids == 0] = 1
+        ids.reshape(-1)[:cap + 1] = 0
+    off, packed, tiles, info = _pack_on_gpu(ids, E, cap, dt)
+    r_off, r_packed, r_tiles, r_nact = O.route_pack(ids, E, cap)
+    assert np.array_equal(off, r_off) and np.array_equal(packed, r_packed)
+    assert np.array_equal(tiles, r_tiles) and info[2] == r_nact and info[0] == 0
+
+
+def test_route_pack_bad_id_sets_error_word():
+    ids = np.array([[0, 1], [5, 2]])
+    _, _, _, info = _pack_on_gpu(ids, 4, 2, "i32")
+    assert info[0] & X.binding.DERR_ROUTE_ID
+
+
+# --------------------------------------------------------------------------- linear
+def _linear_gpu(lw, dev_proj=None):
+    p = dev_proj or X.DeviceProjection(lw.proj)
+    x = to_device(lw.x, lw.act)
+    y = torch.empty((lw.M, lw.proj.out_features), dtype=x.dtype, device="cuda")
+    ws = torch.empty(X.exl3_linear_workspace_bytes(lw.M, lw.proj.in_features,
+                                                    lw.proj.out_features), dtype=torch.uint8,
+                     device="cuda")
+    X.exl3_linear(x, p, y, ws)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("cb", [CB_MUL1, CB_MCG, CB_3INST])
+def test_linear_every_width_and_codebook(K, cb):
+    lw = LinearWorkload(M=5, in_f=640, out_f=384, K=K, cb=cb, act="f16", seed=K * 3 + cb)
+    y = to_f64(_linear_gpu(lw))
+    ref = O.linear(act_to_f64(lw.x, "f16"), lw.proj)
+    assert_close(y, ref, f"linear K={K} cb={cb}")
+
+
+@pytest.mark.parametrize("M,in_f,out_f,act", [(1, 4096, 1408, "bf16"), (37, 1408, 4096, "f16"),
+                                              (128, 512, 256, "bf16"), (200, 256, 128, "f16")])
+def test_linear_shapes(M, in_f, out_f, act):
+    lw = LinearWorkload(M=M, in_f=in_f, out_f=out_f, K=4, cb=CB_MCG, act=act, seed=M)
+    y = to_f64(_linear_gpu(lw))
+    rows = np.arange(min(M, 24))
+    ref = O.linear(act_to_f64(lw.x, act)[rows], lw.proj)
+    assert_close(y[rows], ref, f"linear {M}x{in_f}x{out_f}")
+
+
+def test_linear_rows_are_byte_invariant_across_row_counts():
+    big = LinearWorkload(M=128, in_f=5120, out_f=1536, K=3, cb=CB_MCG, act="bf16", seed=77)
+    dp = X.DeviceProjection(big.proj)
+    y_big = _linear_gpu(big, dp).view(torch.int16).cpu().numpy()
+    for M in (1, 2, 7, 16, 17, 64):
+        small = LinearWorkload(M=M, in_f=5120, out_f=1536, K=3, cb=CB_MCG, act="bf16", seed=77)
+        small.x = big.x[:M]
+        y = _linear_gpu(small, dp).view(torch.int16).cpu().numpy()
+        assert np.array_equal(y, y_big[:M]), M
+
+
+# --------------------------------------------------------------------------- fused layer
+_EXPERTS = {}
+
+
+def _experts(cfg):
+    if cfg not in _EXPERTS:
+        _EXPERTS.clear()
+        torch.cuda.empty_cache()
+        w = MoEWorkload(config(cfg, M=1))
+        _EXPERTS[cfg] = X.DeviceExperts.from_workload(w)
+    return _EXPERTS[cfg]
+
+
+def _stages(w):
+    s = w.spec
+    return X.DeviceStages(w.residual, w.alpha, s.residual_K, s.E)
+
+
+def run_layer(w, experts, capacity=None, stages=None, ws=None):
+    s = w.spec
+    x, ids, rw = moe_inputs(w)
+    out = out_tensor(w)
+    cap = capacity or s.capacity
+    if ws is None:
+        ws = torch.empty(X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter, cap),
+                         dtype=torch.uint8, device="cuda")
+    if stages is None:
+        X.exl3_moe_forward(x, ids, rw, experts, cap, ws, out)
+    else:
+        X.exl3_moe_additive(x, ids, rw, experts, stages, cap, ws, out)
+    torch.cuda.synchronize()
+    assert X.exl3_workspace_error(ws) == 0
+    return out
+
+
+def test_tiny_layer_full_parity():
+    w = MoEWorkload(config(0))
+    out = to_f64(run_layer(w, _experts(0)))
+    assert_close(out, oracle_rows(w), "config 0")
+
+
+def test_tiny_layer_capacity_does_not_change_bytes():
+    w = MoEWorkload(config(0))
+    outs = [run_layer(w, _experts(0), capacity=c).view(torch.int16).cpu().numpy()
+            for c in (1, 3, 5, 512)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("M,tokens", [(1, None), (8, None), (32, [0, 13, 31]),
+                                      (128, [0, 64, 127])])
+def test_decode_layer_parity(M, tokens):
+    w = MoEWorkload(config(1, M=M))
+    out = to_f64(run_layer(w, _experts(1)))
+    rows = np.arange(M) if tokens is None else np.array(tokens)
+    assert_close(out[rows], oracle_rows(w, tokens=rows), f"config 1 M={M}")
+
+
+def test_decode_layer_rows_byte_invariant_across_batch_sizes():
+    ref = None
+    for M in (1, 2, 8, 32, 128):
+        w = MoEWorkload(config(1, M=M))
+        o = run_layer(w, _experts(1)).view(torch.int16).cpu().numpy()
+        if ref is None:
+            ref = o
+        assert np.array_equal(o[:1], ref[:1]), M
+
+
+def test_mixed_width_layer_parity():
+    w = MoEWorkload(config(2))
+    out = to_f64(run_layer(w, _experts(2)))
+    rows = np.array([0, 21, 63])
+    assert_close(out[rows], oracle_rows(w, tokens=rows), "config 2")
+
+
+def test_prefill_layer_parity_sampled():
+    w = MoEWorkload(config(3))
+    out = to_f64(run_layer(w, _experts(3)))
+    rows = np.array([0, 1500, 3071])
+    assert_close(out[rows], oracle_rows(w, tokens=rows), "config 3")
+    assert np.all(np.isfinite(out))
+
+
+def test_additive_layer_parity_and_zero_scale_identity():
+    w = MoEWorkload(config(4))
+    ex = _experts(4)
+    st = _stages(w)
+    out = run_layer(w, ex, stages=st)
+    rows = np.array([0, 255, 511])
+    assert_close(to_f64(out)[rows], oracle_rows(w, tokens=rows), "config 4")
+    # every stage at scale 0: bit-identical to the base-only forward
+    zero = _stages(w)
+    zero.t_scale.zero_()
+    a = run_layer(w, ex, stages=zero).view(torch.int16).cpu().numpy()
+    b = run_layer(w, ex).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- contracts
+def test_host_contract_violation_writes_nothing():
+    import ctypes
+    w = MoEWorkload(config(0))
+    s = w.spec
+    x, ids, rw = moe_inputs(w)
+    out = torch.full((s.M, s.hidden), 3.0, dtype=torch.float16, device="cuda")
+    nbytes = X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter, 4)
+    ws = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    ex = _experts(0)
+    st = ex.struct()
+    lib = X.binding.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call(act=0, hidden=s.hidden, E=s.E, topk=s.topk, cap=4, wsb=nbytes, ids_dt=3, xp=None):
+        return lib.exl3_moe_forward(xp if xp is not None else x.data_ptr(), act, s.M, hidden,
+                                    s.inter, E, topk, ids.data_ptr(), ids_dt, rw.data_ptr(), 0,
+                                    ctypes.byref(st), cap, ws.data_ptr(), wsb, out.data_ptr(),
+                                    stream)
+    assert call(wsb=nbytes - 1) == -6          # workspace short
+    assert call(act=7) == -3                   # unknown dtype
+    assert call(ids_dt=2) == -3                # float ids
+    assert call(hidden=500) == -4              # not a multiple of 128
+    assert call(cap=0) == -7                   # capacity
+    assert call(topk=9) == -7                  # topk > E
+    assert call(E=2000) == -7                  # too many experts
+    assert call(xp=x.data_ptr() + 2) == -5     # misaligned activations
+    assert call(xp=0) == -1                    # null
+    host = torch.zeros(16, dtype=torch.float16).pin_memory()
+    assert call(xp=host.data_ptr()) == -2      # host memory
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0) and torch.all(ws == 0x5A)
+
+
+def test_device_detected_bad_route_zero_fills_output():
+    w = MoEWorkload(config(0))
+    s = w.spec
+    w.ids[3, 1] = s.E + 4
+    x, ids, rw = moe_inputs(w)
+    out = torch.full((s.M, s.hidden), 3.0, dtype=torch.float16, device="cuda")
+    ws = torch.empty(X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter, 4),
+                     dtype=torch.uint8, device="cuda")
+    X.exl3_moe_forward(x, ids, rw, _experts(0), 4, ws, out)
+    torch.cuda.synchronize()
+    assert X.exl3_workspace_error(ws) & X.binding.DERR_ROUTE_ID
+    assert torch.all(out == 0)

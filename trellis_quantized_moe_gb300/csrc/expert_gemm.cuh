@@ -1,0 +1,737 @@
+// Weight-streaming grouped GEMM over EXL3 trellis codes, for the gate/up
+// projections (+ SwiGLU + down-input rotation), the down projection (+ output
+// rotation + route-weighted combine) and the standalone linear.
+//
+// Follows "EXL3 linear and grouped routed experts" (TensorFold #837), "What this
+// changes" (decode straight into tensor-core fragments, grouped experts, gate
+// and up, SwiGLU, down, weighted combine, a width per expert) and "Receipt" (a
+// row's bytes are the same for every row count, K split and member count), and
+// "MoE: Add fused additive EXL3 kernels" (exllamav3 #284), "Summary" (FP32
+// accumulation with output scaling for residual stages).
+//
+// Work item = (row group of <= 8*NRB routes of one expert, 128-output block,
+// range of 512-input chunks).  Each of the 8 warps owns a fixed slice of every
+// chunk, streams that slice's trellis words with cp.async.bulk into its own
+// 3-slot shared-memory ring (one mbarrier per slot), decodes each 16x16 tile
+// in registers straight into mma.sync A fragments and multiplies by the rotated
+// activations (B fragments, rows = routes).
+//
+// Decode: a thread decodes two runs of 4 consecutive trellis positions per
+// tile (output columns g and g+8, input rows 4t..4t+3).  Both runs start at the
+// same bit offset modulo 32, so 3 words + 2 funnel shifts give a 64-bit window
+// from which each 16-bit state is one funnel shift and one shift.  mcg/3inst:
+// the masked product holds two fp16 halves whose sum is the weight; instead of
+// adding them, each half is one element of the MMA's k dimension against a
+// duplicated activation, so the tensor core forms lo*a + hi*a exactly in fp32.
+// mul1: __dp4a sums the four bytes onto the fp16 bit pattern of 1024, giving
+// the exact integer byte sum - 510 after one half2 subtraction; 1/sqrt(21845)
+// is applied to the warp's fp32 partial.
+//
+// Canonical reduction (identical for every row count and every chunk split,
+// hence byte-invariant rows): per 512-input chunk each warp chains its MMAs
+// over its tk slice in ascending order from zero; warp partials are combined
+// by a fixed pairwise tree; chunk partials are added in ascending chunk order.
+// Small launches split chunks over CTAs (fp32 partials in the workspace, the
+// last-arriving CTA adds them in chunk order); large ones keep all chunks in
+// one CTA.  Both perform the same fp32 operations.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace exl3 {
+namespace gemm {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = 2048;           // 8 tiles x 32*K bytes, K <= 8
+constexpr int kActLd = kChunk + 16;        // halves per activation row in smem
+constexpr int kZsLd = kHb + 4;             // floats per row of the z tile
+
+template <int MODE>
+struct ModeTraits {
+    static constexpr int nproj = (MODE == kModeGateUp) ? 2 : 1;
+    static constexpr int group = (MODE == kModeGateUp) ? 4 : 8;   // warps per projection
+    static constexpr int slice_tk = (MODE == kModeGateUp) ? 8 : 4;
+};
+
+template <int MODE, int NRB>
+struct SmemPlan {
+    static constexpr int rows = 8 * NRB;
+    static constexpr int act_bytes_raw = ModeTraits<MODE>::nproj * rows * kActLd * 2;
+    static constexpr int fold_bytes = 4 * NRB * 32 * 32 * 4;
+    static constexpr int act_bytes =
+        ((act_bytes_raw > fold_bytes ? act_bytes_raw : fold_bytes) + 127) / 128 * 128;
+    static constexpr int bar_off = 0;
+    static constexpr int ring_off = 256;
+    static constexpr int act_off = ring_off + kWarps * kSlots * kSlotBytes;
+    static constexpr int zs_off = act_off + act_bytes;
+    static constexpr int zs_bytes = ModeTraits<MODE>::nproj * rows * kZsLd * 4;
+    static constexpr int flag_off = zs_off + zs_bytes;
+    static constexpr int ws_off = flag_off + 16;
+    static constexpr int total = ws_off + kWarps * 128;
+};
+
+struct Item {
+    int e, row0, nrows, nbk, c_begin, c_end, pair;
+};
+
+struct Pass {
+    const uint32_t *trellis;
+    int K, cb, tk0, tk1;
+    float alpha;
+};
+
+template <int MODE, int NRB>
+__device__ __forceinline__ void load_item(const GemmArgs &a, int item, bool split, Item &it)
+{
+    const int pair = split ? item / a.nchunks : item;
+    const int c = split ? item % a.nchunks : 0;
+    it.pair = pair;
+    it.c_begin = c;
+    it.c_end = split ? c + 1 : a.nchunks;
+    const int rgi = pair / a.nb;
+    it.nbk = pair % a.nb;
+    if (MODE == kModeLinear) {
+        it.e = 0;
+        it.row0 = rgi * 8 * NRB;
+        it.nrows = min(8 * NRB, a.M - it.row0);
+    } else {
+        const int4 r = static_cast<const int4 *>(a.rg)[rgi];
+        it.e = r.x;
+        it.row0 = r.y;
+        it.nrows = r.z;
+    }
+}
+
+// The warp's share of (chunk, pass): tk range, trellis, width, codebook.
+// Returns false when the warp streams nothing for it.
+template <int MODE>
+__device__ __forceinline__ bool get_pass(const GemmArgs &a, const Item &it, int chunk, int pass,
+                                         int warp, Pass &ps)
+{
+    using T = ModeTraits<MODE>;
+    const int p = (MODE == kModeGateUp) ? (warp >> 2) : (MODE == kModeDown ? 2 : 0);
+    const int slice = (MODE == kModeGateUp) ? (warp & 3) : warp;
+    const int ntk = a.in_f / 16;
+    ps.tk0 = chunk * kChunkTk + slice * T::slice_tk;
+    ps.tk1 = min(ps.tk0 + T::slice_tk, ntk);
+    if (ps.tk0 >= ps.tk1)
+        return false;
+    if (pass == 0) {
+        if (MODE == kModeLinear) {
+            ps.trellis = a.lin.trellis;
+            ps.K = a.lin.K;
+            ps.cb = a.lin.codebook;
+        } else {
+            const int i = it.e * 3 + p;
+            ps.trellis = reinterpret_cast<const uint32_t *>(a.t_trellis[i]);
+            ps.K = a.t_K[i];
+            ps.cb = a.t_cb[i];
+        }
+        ps.alpha = 1.0f;
+        return true;
+    }
+    const int j = ((pass - 1) * a.E + it.e) * 3 + p;
+    ps.alpha = a.s_scale[j];
+    if (ps.alpha == 0.0f)
+        return false;                       // zero scale: no bytes, no MMA
+    ps.trellis = reinterpret_cast<const uint32_t *>(a.s_trellis[j]);
+    ps.K = a.s_K[j];
+    ps.cb = EXL3_CB_MCG;
+    return true;
+}
+
+// Enumerates, in consumption order, the trellis segments (one tk row of the 8
+// tiles of a 128-output block) that one warp streams.
+struct Producer {
+    int item, chunk, pass, tk, n_items;
+    bool split, have, done;
+    Item it;
+    Pass ps;
+};
+
+template <int MODE, int NRB, bool ADD>
+__device__ __forceinline__ void producer_init(const GemmArgs &a, Producer &P, int n_items,
+                                              bool split)
+{
+    P.n_items = n_items;
+    P.split = split;
+    P.item = blockIdx.x;
+    P.have = false;
+    P.done = P.item >= n_items;
+    P.pass = -1;
+    if (!P.done) {
+        load_item<MODE, NRB>(a, P.item, split, P.it);
+        P.chunk = P.it.c_begin;
+    }
+}
+
+template <int MODE, int NRB, bool ADD>
+__device__ __forceinline__ bool producer_next(const GemmArgs &a, Producer &P, int warp,
+                                              const uint32_t **src, uint32_t *bytes)
+{
+    const int npass = ADD ? a.num_stages : 1;
+    while (!P.done) {
+        if (P.have && P.tk < P.ps.tk1) {
+            *src = P.ps.trellis +
+                   ((size_t)P.tk * (a.out_f / 16) + (size_t)P.it.nbk * 8) * (8 * P.ps.K);
+            *bytes = 256u * P.ps.K;
+            P.tk++;
+            return true;
+        }
+        P.have = false;
+        if (++P.pass < npass) {
+            P.have = get_pass<MODE>(a, P.it, P.chunk, P.pass, warp, P.ps);
+            P.tk = P.ps.tk0;
+            continue;
+        }
+        P.pass = -1;
+        if (++P.chunk < P.it.c_end)
+            continue;
+        P.item += gridDim.x;
+        if (P.item >= P.n_items) {
+            P.done = true;
+            return false;
+        }
+        load_item<MODE, NRB>(a, P.item, P.split, P.it);
+        P.chunk = P.it.c_begin;
+    }
+    return false;
+}
+
+// Per-warp stream state.  The producer cursor lives in shared memory and only
+// lane 0 advances it and issues copies; the consumer only counts slots.
+struct WarpStream {
+    Producer P;
+    uint32_t issued;
+    int dead;
+};
+
+static_assert(sizeof(WarpStream) <= 128, "WarpStream slot");
+
+struct Ring {
+    uint64_t *bar;
+    uint8_t *buf;
+    WarpStream *ws;
+    uint32_t head;
+    bool dead;
+};
+
+template <int MODE, int NRB, bool ADD>
+__device__ __forceinline__ void ring_issue(Ring &r, const GemmArgs &a, int warp)
+{
+    if ((threadIdx.x & 31) != 0)
+        return;
+    WarpStream *w = r.ws;
+    const uint32_t *src;
+    uint32_t bytes;
+    if (w->dead)
+        return;
+    if (producer_next<MODE, NRB, ADD>(a, w->P, warp, &src, &bytes)) {
+        const int slot = w->issued % kSlots;
+        mbar_arrive_expect_tx(&r.bar[slot], bytes);
+        bulk_g2s(r.buf + slot * kSlotBytes, src, bytes, &r.bar[slot]);
+        w->issued++;
+    }
+}
+
+__device__ __forceinline__ const uint32_t *ring_wait(Ring &r, int32_t *hdr)
+{
+    if (r.dead)
+        return nullptr;
+    const int slot = r.head % kSlots;
+    const uint32_t parity = (r.head / kSlots) & 1u;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&r.bar[slot], parity));
+    if (!ok) {
+        r.dead = true;
+        if ((threadIdx.x & 31) == 0) {
+            r.ws->dead = 1;
+            set_error(hdr, EXL3_DERR_TIMEOUT);
+        }
+        return nullptr;
+    }
+    return reinterpret_cast<const uint32_t *>(r.buf + slot * kSlotBytes);
+}
+
+template <int MODE, int NRB, bool ADD>
+__device__ __forceinline__ void ring_release(Ring &r, const GemmArgs &a, int warp)
+{
+    __syncwarp();
+    r.head++;
+    ring_issue<MODE, NRB, ADD>(r, a, warp);
+}
+
+// Before exit: wait (bounded) for copies still in flight into this warp's ring.
+__device__ __forceinline__ void ring_drain(Ring &r)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) != 0)
+        return;
+    uint32_t h = r.head;
+    while (h < r.ws->issued) {
+        const int slot = h % kSlots;
+        mbar_wait(&r.bar[slot], (h / kSlots) & 1u);
+        h++;
+    }
+}
+
+__device__ __forceinline__ uint32_t hsub_1534(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    h = __hsub2(h, __half2(__ushort_as_half(0x65FE), __ushort_as_half(0x65FE)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Decode + MMA over the warp's tk slice of one (chunk, pass).
+template <int K, bool MUL1, int MODE, int NRB, bool ADD>
+__device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
+                                         const GemmArgs &a, int warp, const Pass &ps,
+                                         int chunk, const uint16_t *act_s)
+{
+    constexpr int NWD = 8 * K;                // 32-bit words per tile
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int start = (16 * g + 4 * t + 1) * K - 16;   // first bit of run A's window
+    const int w0 = start >> 5;                          // floor (may be -1)
+    const int o = start & 31;
+    const int oA0 = (w0 + NWD) % NWD, oA1 = (w0 + 1 + NWD) % NWD, oA2 = (w0 + 2 + NWD) % NWD;
+    const int oB0 = (w0 + 4 * K) % NWD, oB1 = (w0 + 4 * K + 1) % NWD, oB2 = (w0 + 4 * K + 2) % NWD;
+    const uint32_t mul = MUL1 ? 0x83DCD12Du : (ps.cb == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
+    const uint32_t add = (!MUL1 && ps.cb == EXL3_CB_3INST) ? 64248484u : 0u;
+
+    for (int tk = ps.tk0; tk < ps.tk1; tk++) {
+        const uint32_t *seg = ring_wait(ring, a.hdr);
+        if (seg != nullptr) {
+            const uint32_t seg_s = smem_addr(seg);
+            const int kcol = (tk - chunk * kChunkTk) * 16 + 4 * t;
+            uint32_t bf[NRB][4];
+#pragma unroll
+            for (int nb = 0; nb < NRB; nb++) {
+                const uint2 v =
+                    *reinterpret_cast<const uint2 *>(act_s + (8 * nb + g) * kActLd + kcol);
+                if (MUL1) {
+                    bf[nb][0] = v.x;
+                    bf[nb][1] = v.y;
+                } else {
+                    bf[nb][0] = prmt(v.x, v.x, 0x1010);
+                    bf[nb][1] = prmt(v.x, v.x, 0x3232);
+                    bf[nb][2] = prmt(v.y, v.y, 0x1010);
+                    bf[nb][3] = prmt(v.y, v.y, 0x3232);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t tw = seg_s + j * NWD * 4;
+                const uint32_t a0 = lds_u32(tw + 4 * oA0), a1 = lds_u32(tw + 4 * oA1),
+                               a2 = lds_u32(tw + 4 * oA2);
+                const uint32_t b0 = lds_u32(tw + 4 * oB0), b1 = lds_u32(tw + 4 * oB1),
+                               b2 = lds_u32(tw + 4 * oB2);
+                const uint32_t XA0 = __funnelshift_l(a1, a0, o), XA1 = __funnelshift_l(a2, a1, o);
+                const uint32_t XB0 = __funnelshift_l(b1, b0, o), XB1 = __funnelshift_l(b2, b1, o);
+                uint32_t sA[4], sB[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    sA[i] = __funnelshift_l(XA1, XA0, i * K) >> 16;
+                    sB[i] = __funnelshift_l(XB1, XB0, i * K) >> 16;
+                }
+                if (MUL1) {
+                    uint32_t dA[4], dB[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        dA[i] = __dp4a(sA[i] * mul, 0x01010101u, 0x6400u);
+                        dB[i] = __dp4a(sB[i] * mul, 0x01010101u, 0x6400u);
+                    }
+                    const uint32_t A0 = hsub_1534(prmt(dA[0], dA[1], 0x5410));
+                    const uint32_t A1 = hsub_1534(prmt(dB[0], dB[1], 0x5410));
+                    const uint32_t A2 = hsub_1534(prmt(dA[2], dA[3], 0x5410));
+                    const uint32_t A3 = hsub_1534(prmt(dB[2], dB[3], 0x5410));
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++)
+                        mma_16816(acc[nb][j], A0, A1, A2, A3, bf[nb][0], bf[nb][1]);
+                } else {
+                    uint32_t xA[4], xB[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        xA[i] = lop_mask_xor(sA[i] * mul + add);
+                        xB[i] = lop_mask_xor(sB[i] * mul + add);
+                    }
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++) {
+                        mma_16816(acc[nb][j], xA[0], xB[0], xA[1], xB[1], bf[nb][0], bf[nb][1]);
+                        mma_16816(acc[nb][j], xA[2], xB[2], xA[3], xB[3], bf[nb][2], bf[nb][3]);
+                    }
+                }
+            }
+        }
+        ring_release<MODE, NRB, ADD>(ring, a, warp);
+    }
+}
+
+template <int MODE, int NRB, bool ADD>
+__device__ __forceinline__ void dispatch_pass(float (&acc)[NRB][8][4], Ring &ring,
+                                              const GemmArgs &a, int warp, const Pass &ps,
+                                              int chunk, const uint16_t *act_s)
+{
+    const bool mul1 = ps.cb == EXL3_CB_MUL1;
+#define EXL3_K_CASE(KK)                                                                     \
+    case KK:                                                                                \
+        if (mul1)                                                                           \
+            run_pass<KK, true, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s);  \
+        else                                                                                \
+            run_pass<KK, false, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s); \
+        break;
+    switch (ps.K) {
+        EXL3_K_CASE(1)
+        EXL3_K_CASE(2)
+        EXL3_K_CASE(3)
+        EXL3_K_CASE(4)
+        EXL3_K_CASE(5)
+        EXL3_K_CASE(6)
+        EXL3_K_CASE(7)
+        EXL3_K_CASE(8)
+        default:
+            break;
+    }
+#undef EXL3_K_CASE
+}
+
+constexpr int kPartStride = kRowGroup * kHb;   // floats per (pair, chunk, projection) partial
+
+// Element e of the fragment-ordered partials [nproj][nb][j][r][lane] -> its
+// index in zs[nproj][ROWS][kZsLd] (row = route, column = output in the block).
+template <int ROWS>
+__device__ __forceinline__ int zs_index(int e, int frag)
+{
+    const int p = e / (frag * 32);
+    const int i = e % (frag * 32);
+    const int lane = i & 31, q = i >> 5;
+    const int r = q & 3, j = (q >> 2) & 7, nb = q >> 5;
+    const int row = 8 * nb + 2 * (lane & 3) + (r & 1);
+    const int col = 16 * j + (lane >> 2) + 8 * (r >> 1);
+    return (p * ROWS + row) * kZsLd + col;
+}
+
+template <int MODE, int NRB, bool ADD>
+__global__ void __launch_bounds__(kThreads, NRB == 1 ? 2 : 1) k_expert_gemm(GemmArgs a)
+{
+    using T = ModeTraits<MODE>;
+    using S = SmemPlan<MODE, NRB>;
+    constexpr int ROWS = 8 * NRB;
+    constexpr int FRAG = NRB * 32;           // accumulator floats per lane
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::bar_off);
+    uint8_t *ring_base = smem + S::ring_off;
+    uint16_t *act_s = reinterpret_cast<uint16_t *>(smem + S::act_off);
+    float *fold = reinterpret_cast<float *>(smem + S::act_off);   // aliases act_s
+    float *zs = reinterpret_cast<float *>(smem + S::zs_off);
+    int *s_flag = reinterpret_cast<int *>(smem + S::flag_off);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    int n_items;
+    bool split;
+    if (MODE == kModeLinear) {
+        n_items = a.n_items_host;
+        split = a.split_host != 0;
+    } else {
+        n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
+        split = a.hdr[MODE == kModeGateUp ? kHdrSplit1 : kHdrSplit2] != 0;
+        if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
+            // device-detected contract violation: zero-filled output
+            const size_t n = (size_t)a.M_tokens * a.out_f;
+            for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n;
+                 i += (size_t)gridDim.x * kThreads)
+                reinterpret_cast<uint16_t *>(a.out)[i] = 0;
+            return;
+        }
+    }
+    if ((int)blockIdx.x >= n_items)
+        return;
+
+    Ring ring;
+    ring.bar = bars + warp * kSlots;
+    ring.buf = ring_base + warp * kSlots * kSlotBytes;
+    ring.ws = reinterpret_cast<WarpStream *>(smem + S::ws_off) + warp;
+    ring.head = 0;
+    ring.dead = false;
+    if (lane == 0) {
+        for (int s = 0; s < kSlots; s++)
+            mbar_init(&ring.bar[s], 1);
+        fence_mbar_init();
+        producer_init<MODE, NRB, ADD>(a, ring.ws->P, n_items, split);
+        ring.ws->issued = 0;
+        ring.ws->dead = 0;
+    }
+    __syncwarp();
+    for (int s = 0; s < kSlots; s++)
+        ring_issue<MODE, NRB, ADD>(ring, a, warp);
+
+    const int npass = ADD ? a.num_stages : 1;
+    const int my_proj = (MODE == kModeGateUp) ? (warp >> 2) : 0;
+    const bool root = (warp % T::group) == 0;
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        Item it;
+        load_item<MODE, NRB>(a, item, split, it);
+
+        for (int chunk = it.c_begin; chunk < it.c_end; chunk++) {
+            // ---- activations of this chunk: [nproj][ROWS][512] fp16
+            named_barrier(1, kThreads);
+            {
+                const int c0 = chunk * kChunk;
+                const int nvec = T::nproj * ROWS * (kChunk / 8);
+                for (int v = tid; v < nvec; v += kThreads) {
+                    const int col = (v % (kChunk / 8)) * 8;
+                    const int r = (v / (kChunk / 8)) % ROWS;
+                    const int p = v / (ROWS * (kChunk / 8));
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (r < it.nrows && c0 + col < a.in_f) {
+                        const uint16_t *src = a.act + (size_t)(it.row0 + r) * a.act_row_stride +
+                                              (size_t)p * a.in_f + c0 + col;
+                        val = __ldg(reinterpret_cast<const uint4 *>(src));
+                    }
+                    *reinterpret_cast<uint4 *>(act_s + (p * ROWS + r) * kActLd + col) = val;
+                }
+            }
+            named_barrier(1, kThreads);
+
+            // ---- this warp's partial over its slice, base + residual stages
+            float acc[NRB][8][4];
+#pragma unroll
+            for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+#pragma unroll
+                    for (int r = 0; r < 4; r++)
+                        acc[nb][j][r] = 0.0f;
+            const uint16_t *act_p = act_s + my_proj * ROWS * kActLd;
+            for (int pass = 0; pass < npass; pass++) {
+                Pass ps;
+                if (!get_pass<MODE>(a, it, chunk, pass, warp, ps))
+                    continue;
+                if (!ADD) {
+                    dispatch_pass<MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_p);
+                    if (ps.cb == EXL3_CB_MUL1) {
+#pragma unroll
+                        for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                            for (int j = 0; j < 8; j++)
+#pragma unroll
+                                for (int r = 0; r < 4; r++)
+                                    acc[nb][j][r] *= kInvSqrtMul1;
+                    }
+                } else {
+                    float tmp[NRB][8][4];
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+#pragma unroll
+                            for (int r = 0; r < 4; r++)
+                                tmp[nb][j][r] = 0.0f;
+                    dispatch_pass<MODE, NRB, ADD>(tmp, ring, a, warp, ps, chunk, act_p);
+                    const float f = (ps.cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+#pragma unroll
+                            for (int r = 0; r < 4; r++) {
+                                if (pass == 0)
+                                    acc[nb][j][r] = (f == 1.0f) ? tmp[nb][j][r] : tmp[nb][j][r] * f;
+                                else
+                                    acc[nb][j][r] = __fmaf_rn(ps.alpha, tmp[nb][j][r], acc[nb][j][r]);
+                            }
+                }
+            }
+
+            // ---- fixed pairwise tree over the warps of each projection
+#pragma unroll
+            for (int s = 1; s < T::group; s <<= 1) {
+                named_barrier(1, kThreads);
+                const int wl = warp % T::group;
+                if (wl % (2 * s) == s) {
+                    float *slot = fold + ((warp - s) / (2 * s)) * FRAG * 32;
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+#pragma unroll
+                            for (int r = 0; r < 4; r++)
+                                slot[((nb * 8 + j) * 4 + r) * 32 + lane] = acc[nb][j][r];
+                }
+                named_barrier(1, kThreads);
+                if (wl % (2 * s) == 0) {
+                    const float *slot = fold + (warp / (2 * s)) * FRAG * 32;
+#pragma unroll
+                    for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+#pragma unroll
+                            for (int r = 0; r < 4; r++)
+                                acc[nb][j][r] = acc[nb][j][r] + slot[((nb * 8 + j) * 4 + r) * 32 + lane];
+                }
+            }
+
+            // ---- chunk partial of each projection: root warp -> shared memory
+            //      (fragment order), then elementwise: running sum in zs, or
+            //      out to the workspace when chunks are split over CTAs
+            named_barrier(1, kThreads);
+            if (root) {
+                float *pb = fold + my_proj * FRAG * 32;
+#pragma unroll
+                for (int nb = 0; nb < NRB; nb++)
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+#pragma unroll
+                        for (int r = 0; r < 4; r++)
+                            pb[((nb * 8 + j) * 4 + r) * 32 + lane] = acc[nb][j][r];
+            }
+            named_barrier(1, kThreads);
+            if (split) {
+                float *dst = a.part + (size_t)(it.pair * a.nchunks + chunk) * T::nproj * kPartStride;
+                for (int e = tid; e < T::nproj * FRAG * 32; e += kThreads)
+                    dst[(e / (FRAG * 32)) * kPartStride + e % (FRAG * 32)] = fold[e];
+            } else {
+                const bool first = chunk == it.c_begin;
+                for (int e = tid; e < T::nproj * FRAG * 32; e += kThreads) {
+                    float &zz = zs[zs_index<ROWS>(e, FRAG)];
+                    zz = first ? fold[e] : zz + fold[e];
+                }
+            }
+        }
+
+        if (split) {
+            // last CTA of this (row group, block) adds the chunk partials in order
+            __threadfence();
+            named_barrier(1, kThreads);
+            if (tid == 0) {
+                const int old = atomicAdd(&a.cnt_split[it.pair], 1);
+                *s_flag = (old == a.nchunks - 1);
+            }
+            named_barrier(1, kThreads);
+            if (*s_flag == 0)
+                continue;
+            __threadfence();
+            const float *src = a.part + (size_t)it.pair * a.nchunks * T::nproj * kPartStride;
+            for (int e = tid; e < T::nproj * FRAG * 32; e += kThreads) {
+                const int off = (e / (FRAG * 32)) * kPartStride + e % (FRAG * 32);
+                float run = 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < a.nchunks; c++) {
+                    const float v = __ldcg(src + (size_t)c * T::nproj * kPartStride + off);
+                    run = (c == 0) ? v : run + v;
+                }
+                zs[zs_index<ROWS>(e, FRAG)] = run;
+            }
+            if (tid == 0)
+                a.cnt_split[it.pair] = 0;
+        }
+        named_barrier(1, kThreads);
+
+        // ---- epilogue: one warp per row, lane l owns outputs 4l..4l+3 of the block
+        const int col = it.nbk * kHb + 4 * lane;
+        for (int r = warp; r < it.nrows; r += kWarps) {
+            if (MODE == kModeGateUp) {
+                const int e = it.e;
+                float gv[4], uv[4], sv[4], sc[4], h[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    gv[i] = zs[r * kZsLd + 4 * lane + i];
+                    uv[i] = zs[(ROWS + r) * kZsLd + 4 * lane + i];
+                }
+                warp_hadamard128(gv);
+                warp_hadamard128(uv);
+                load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 0]), col, sv);
+                load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 0]), col, sc);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    gv[i] = gv[i] * kInvSqrt128 * sv[i] * sc[i];
+                load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 1]), col, sv);
+                load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 1]), col, sc);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    uv[i] = uv[i] * kInvSqrt128 * sv[i] * sc[i];
+                load_half4(reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + 2]), col, sv);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    h[i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i] * sv[i];
+                warp_hadamard128(h);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    h[i] *= kInvSqrt128;
+                store_act4(a.ad, (size_t)(it.row0 + r) * a.out_f + col, EXL3_F16, h);
+            } else {
+                const uint16_t *svh, *scl;
+                if (MODE == kModeLinear) {
+                    svh = a.lin.svh;
+                    scl = a.lin.scale;
+                } else {
+                    svh = reinterpret_cast<const uint16_t *>(a.t_svh[it.e * 3 + 2]);
+                    scl = reinterpret_cast<const uint16_t *>(a.t_scale[it.e * 3 + 2]);
+                }
+                float z[4], sv[4], sc[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    z[i] = zs[r * kZsLd + 4 * lane + i];
+                warp_hadamard128(z);
+                load_half4(svh, col, sv);
+                load_half4(scl, col, sc);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
+                if (MODE == kModeLinear) {
+                    store_act4(a.out, (size_t)(it.row0 + r) * a.out_f + col, a.act_dtype, z);
+                } else {
+                    const int f = a.packed[it.row0 + r];
+                    const int tok = f / a.topk;
+                    *reinterpret_cast<float4 *>(a.stage + (size_t)f * a.out_f + col) =
+                        make_float4(z[0], z[1], z[2], z[3]);
+                    __threadfence();
+                    __syncwarp();
+                    int old = 0;
+                    if (lane == 0)
+                        old = atomicAdd(&a.cnt_comb[tok * a.nb + it.nbk], 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old == a.topk - 1) {
+                        // every route of this token has its block: combine in j order
+                        __threadfence();
+                        float o4[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int j = 0; j < a.topk; j++) {
+                            const float w = load_act(a.rw, (size_t)tok * a.topk + j, a.rw_dtype);
+                            const float4 d = __ldcg(reinterpret_cast<const float4 *>(
+                                a.stage + ((size_t)tok * a.topk + j) * a.out_f + col));
+                            o4[0] = __fmaf_rn(w, d.x, o4[0]);
+                            o4[1] = __fmaf_rn(w, d.y, o4[1]);
+                            o4[2] = __fmaf_rn(w, d.z, o4[2]);
+                            o4[3] = __fmaf_rn(w, d.w, o4[3]);
+                        }
+                        store_act4(a.out, (size_t)tok * a.out_f + col, a.act_dtype, o4);
+                        if (lane == 0)
+                            a.cnt_comb[tok * a.nb + it.nbk] = 0;
+                    }
+                }
+            }
+        }
+        named_barrier(1, kThreads);
+    }
+    ring_drain(ring);
+}
+
+template <int MODE, int NRB, bool ADD>
+cudaError_t launch_one(const GemmArgs &a, int grid, cudaStream_t s)
+{
+    k_expert_gemm<MODE, NRB, ADD><<<grid, kThreads, SmemPlan<MODE, NRB>::total, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MODE, int NRB, bool ADD>
+cudaError_t set_attr_one()
+{
+    return cudaFuncSetAttribute(k_expert_gemm<MODE, NRB, ADD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SmemPlan<MODE, NRB>::total);
+}
+
+}  // namespace gemm
+}  // namespace exl3

@@ -1,0 +1,25 @@
+// Gate/up projections of the grouped experts with the fused SwiGLU and
+// down-input rotation epilogue (see expert_gemm.cuh).
+#include "expert_gemm.cuh"
+
+namespace exl3 {
+
+cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int grid,
+                              cudaStream_t s)
+{
+    if (additive)
+        return gemm::launch_one<kModeGateUp, 1, true>(a, grid, s);
+    if (nrb == 2)
+        return gemm::launch_one<kModeGateUp, 2, false>(a, grid, s);
+    return gemm::launch_one<kModeGateUp, 1, false>(a, grid, s);
+}
+
+cudaError_t gemm_gateup_set_attributes()
+{
+    cudaError_t e = gemm::set_attr_one<kModeGateUp, 1, true>();
+    if (e == cudaSuccess)
+        e = gemm::set_attr_one<kModeGateUp, 1, false>();
+    return e != cudaSuccess ? e : gemm::set_attr_one<kModeGateUp, 2, false>();
+}
+
+}  // namespace exl3

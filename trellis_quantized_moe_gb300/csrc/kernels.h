@@ -1,0 +1,99 @@
+// Kernel argument structs and launchers (host <-> device interface of the
+// library; internal, not part of the C ABI).
+#pragma once
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#include "../../include/exl3.h"
+#include "plan.h"
+
+#ifndef __CUDACC__
+struct int4_host { int x, y, z, w; };
+#endif
+
+namespace exl3 {
+
+struct RoutePackArgs {
+    const void *ids;
+    int R, E, capacity, rg_size, nw;
+    int32_t *offsets, *packed, *tiles, *info;
+    // fused-layer planning (plan != 0)
+    int plan;
+    void *rg;                       // int4 [max_rg] = (expert, first row, rows, 0)
+    int nb1, nb2, nchunks1, nchunks2, split_pairs1, split_pairs2, num_sms;
+    const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
+    const int32_t *t_K, *t_cb;
+    int num_stages;
+    const int64_t *s_trellis;
+    const float *s_scale;
+    const int32_t *s_K;
+};
+
+struct RotateArgs {
+    const void *x;
+    int act_dtype, rows, width, nproj;
+    // fused layer: row i is packed slot i, token = packed[i] / topk, suh from the table
+    const int32_t *packed;
+    const void *ids;
+    int ids_dtype, topk;
+    const int64_t *t_suh;
+    // linear: row i is token i, one suh
+    const uint16_t *suh;
+    uint16_t *out;                  // fp16 [rows][nproj][width]
+    int32_t *hdr;                   // skip everything when the error word is set
+    int32_t *zero;                  // words to clear
+    int nzero;
+    int32_t *hdr_reset;             // linear: header to reset (error word)
+};
+
+enum GemmMode { kModeGateUp = 0, kModeDown = 1, kModeLinear = 2 };
+
+struct GemmArgs {
+    int act_dtype;
+    int in_f, out_f, nb, nchunks;
+    int32_t *hdr;
+    const void *rg;                 // int4 row groups (fused layer)
+    // linear: host-planned work
+    int M, n_items_host, split_host;
+    const uint16_t *act;            // fp16 rows (rotated activations)
+    long act_row_stride;            // halves between rows
+    // expert tables (fused layer)
+    const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
+    const int32_t *t_K, *t_cb;
+    // linear projection
+    exl3_proj lin;
+    // additive stages
+    int num_stages, E;
+    const int64_t *s_trellis;
+    const float *s_scale;
+    const int32_t *s_K;
+    // split partials
+    float *part;
+    int32_t *cnt_split;
+    // outputs
+    uint16_t *ad;                   // gate/up: fp16 [R][inter]
+    float *stage;                   // down: fp32 [R][hidden]
+    const int32_t *packed;
+    int topk;
+    const void *rw;
+    int rw_dtype;
+    int32_t *cnt_comb;
+    void *out;                      // down: [M][hidden] act; linear: [M][out] act
+    int M_tokens;
+};
+
+int route_pack_hist_warps(int E);
+cudaError_t launch_route_pack(const RoutePackArgs &a, int ids_dtype, cudaStream_t s);
+cudaError_t route_pack_set_attributes();
+cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s);
+cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t gemm_gateup_set_attributes();
+cudaError_t gemm_down_set_attributes();
+cudaError_t gemm_linear_set_attributes();
+// resident CTAs per SM of the GEMM kernels for 8- and 16-row items
+constexpr int kGemmCtasPerSm8 = 2;
+constexpr int kGemmCtasPerSm16 = 1;
+
+}  // namespace exl3

@@ -1,0 +1,263 @@
+// Route histogram, exclusive scan and stable packing of (token, expert) routes
+// into per-expert spans, capacity tiles and row groups ("MoE: Add fused additive
+// EXL3 kernels", exllamav3 #284, "Summary" and "Relationship to #246").
+//
+// One CTA of 1024 threads.  The routes are cut into nw contiguous chunks, one
+// per warp.  Pass 1 builds a per-warp histogram in shared memory; the expert
+// scan turns (expert-major, warp-minor) counts into per-warp write cursors;
+// pass 2 walks each chunk in order, 32 routes at a time, ranking equal ids
+// inside the step with __match_any_sync.  The result is the unique stable
+// order (ascending flat route index inside each expert's span).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+// Exclusive scan of v over the block (one value per thread); returns the
+// exclusive prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int *warp_sums, int *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d)
+            x += y;
+    }
+    if (lane == 31)
+        warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int s = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, d);
+            if (lane >= d)
+                s += y;
+        }
+        warp_sums[lane] = s - w;          // exclusive warp offsets
+        if (lane == 31)
+            warp_sums[32] = s;
+    }
+    __syncthreads();
+    int r = warp_sums[warp] + x - v;
+    *total = warp_sums[32];
+    __syncthreads();
+    return r;
+}
+
+template <typename IdT>
+__device__ __forceinline__ long long read_id(const IdT *ids, int f)
+{
+    return static_cast<long long>(ids[f]);
+}
+
+}  // namespace
+
+template <typename IdT>
+__global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
+{
+    extern __shared__ int smem_i[];
+    const IdT *ids = static_cast<const IdT *>(a.ids);
+    const int E = a.E, R = a.R;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+    const int nw = a.nw;                       // warps holding a histogram row
+    int *hist = smem_i;                        // [nw][E]
+    __shared__ int s_warp[40];
+    __shared__ int s_err;
+
+    for (int i = tid; i < nw * E; i += kThreads)
+        hist[i] = 0;
+    if (tid == 0) {
+        s_err = 0;
+        a.info[kHdrError] = 0;
+    }
+    __syncthreads();
+
+    // chunk of each warp: whole 32-route steps
+    const int steps = (R + 31) / 32;
+    const int per_warp = (steps + nw - 1) / nw;
+    const int f_begin = warp * per_warp * 32;
+    const int f_end = min(R, f_begin + per_warp * 32);
+
+    // pass 1: validate and count
+    if (warp < nw) {
+        for (int f = f_begin + lane; f < f_end; f += 32) {
+            long long e = read_id(ids, f);
+            if (e < 0 || e >= E)
+                s_err = 1;
+            else
+                atomicAdd(&hist[warp * E + (int)e], 1);
+        }
+    }
+    __syncthreads();
+    if (s_err) {
+        if (tid == 0) {
+            a.info[kHdrError] |= EXL3_DERR_ROUTE_ID;
+            a.info[kHdrNTiles] = 0;
+            a.info[kHdrNumActive] = 0;
+            if (a.plan) {
+                a.info[kHdrNRg] = 0;
+                a.info[kHdrNItems1] = 0;
+                a.info[kHdrNItems2] = 0;
+            }
+        }
+        return;
+    }
+
+    // per-expert totals, spans and tile / row-group counts
+    int cnt = 0;
+    if (tid < E)
+        for (int w = 0; w < nw; w++)
+            cnt += hist[w * E + tid];
+    int total;
+    const int off = block_exclusive_scan(tid < E ? cnt : 0, s_warp, &total);
+    const int ntile_e = (tid < E) ? (cnt + a.capacity - 1) / a.capacity : 0;
+    int ntiles;
+    const int tile_off = block_exclusive_scan(ntile_e, s_warp, &ntiles);
+    int nrg_e = 0;
+    if (tid < E && a.plan) {
+        for (int s = 0; s < ntile_e; s++) {
+            int len = min(a.capacity, cnt - s * a.capacity);
+            nrg_e += (len + a.rg_size - 1) / a.rg_size;
+        }
+    }
+    int n_rg;
+    const int rg_off = block_exclusive_scan(nrg_e, s_warp, &n_rg);
+    int nact;
+    block_exclusive_scan((tid < E && cnt > 0) ? 1 : 0, s_warp, &nact);
+    if (tid < E) {
+        a.offsets[tid] = off;
+        // per-warp cursors: expert-major, warp-minor
+        int run = off;
+        for (int w = 0; w < nw; w++) {
+            int c = hist[w * E + tid];
+            hist[w * E + tid] = run;
+            run += c;
+        }
+    }
+    if (tid == 0)
+        a.offsets[E] = total;
+    __syncthreads();
+
+    // pass 2: stable placement
+    if (warp < nw) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int f0 = f_begin; f0 < f_end; f0 += 32) {
+            const int f = f0 + lane;
+            const bool valid = f < f_end;
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            int e = valid ? (int)read_id(ids, f) : -1;
+            unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (valid) {
+                peers &= vmask;
+                int rank = __popc(peers & lt);
+                int base = hist[warp * E + e];
+                a.packed[base + rank] = f;
+            }
+            __syncwarp();
+            if (valid && (peers & lt) == 0)          // lowest lane of its group
+                hist[warp * E + e] += __popc(peers);
+            __syncwarp();
+        }
+    }
+
+    // capacity tiles (and row groups for the fused layer)
+    if (tid < E && cnt > 0) {
+        for (int s = 0; s < ntile_e; s++) {
+            const int start = off + s * a.capacity;
+            const int len = min(a.capacity, cnt - s * a.capacity);
+            int *t = a.tiles + 3 * (tile_off + s);
+            t[0] = tid; t[1] = start; t[2] = len;
+        }
+        if (a.plan) {
+            int k = rg_off;
+            for (int s = 0; s < ntile_e; s++) {
+                const int start = off + s * a.capacity;
+                const int len = min(a.capacity, cnt - s * a.capacity);
+                for (int r = 0; r < len; r += a.rg_size)
+                    static_cast<int4 *>(a.rg)[k++] = make_int4(tid, start + r, min(a.rg_size, len - r), 0);
+            }
+        }
+    }
+
+    // the fused layer: validate the tables of every expert that receives routes
+    if (a.plan && tid < E && cnt > 0) {
+        bool bad = false;
+        for (int p = 0; p < 3; p++) {
+            const int i = tid * 3 + p;
+            const int K = a.t_K[i], cb = a.t_cb[i];
+            const long long tr = a.t_trellis[i];
+            bad |= K < 1 || K > 8 || cb < 0 || cb > 2 || tr == 0 || (tr & 15);
+            bad |= a.t_suh[i] == 0 || (a.t_suh[i] & 7) || a.t_svh[i] == 0 || (a.t_svh[i] & 7) ||
+                   a.t_scale[i] == 0 || (a.t_scale[i] & 7);
+            for (int s = 1; s < a.num_stages; s++) {
+                const int j = ((s - 1) * E + tid) * 3 + p;
+                if (a.s_scale[j] != 0.0f) {
+                    const int Ks = a.s_K[j];
+                    const long long ts = a.s_trellis[j];
+                    bad |= Ks < 1 || Ks > 8 || ts == 0 || (ts & 15);
+                }
+            }
+        }
+        if (bad)
+            s_err = 2;
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        a.info[kHdrNTiles] = ntiles;
+        a.info[kHdrNumActive] = nact;
+        if (a.plan) {
+            if (s_err) {
+                a.info[kHdrError] |= EXL3_DERR_TABLE;
+                n_rg = 0;
+            }
+            a.info[kHdrNRg] = n_rg;
+            const int pairs1 = n_rg * a.nb1, pairs2 = n_rg * a.nb2;
+            const int lim = min(kSplitMaxPairs, 4 * a.num_sms);
+            const int split1 = a.nchunks1 > 1 && pairs1 <= min(lim, a.split_pairs1);
+            const int split2 = a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
+            a.info[kHdrSplit1] = split1;
+            a.info[kHdrSplit2] = split2;
+            a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
+            a.info[kHdrNItems2] = split2 ? pairs2 * a.nchunks2 : pairs2;
+        }
+    }
+}
+
+int route_pack_hist_warps(int E)
+{
+    int nw = 16384 / (E > 0 ? E : 1);
+    return nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+}
+
+cudaError_t launch_route_pack(const RoutePackArgs &a, int ids_dtype, cudaStream_t s)
+{
+    const size_t smem = (size_t)a.nw * a.E * sizeof(int);
+    if (ids_dtype == EXL3_I64) {
+        k_route_pack<int64_t><<<1, kThreads, smem, s>>>(a);
+    } else {
+        k_route_pack<int32_t><<<1, kThreads, smem, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t route_pack_set_attributes()
+{
+    const int max_dyn = 16384 * (int)sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(k_route_pack<int32_t>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+    if (e != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(k_route_pack<int64_t>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+}
+
+}  // namespace exl3
