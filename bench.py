@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Benchmark of the fused EXL3 routed-expert MoE layer on GB300.
+
+Headline: the decode-shaped layer (hidden 5120, inter 1536, 192 experts, top-8,
+K=3 mcg, bf16) at M=1 token: routed tokens/s of one layer call, with the L2
+flushed (256 MB write) before every timed step so the trellis words come from
+HBM.  The same line carries the M = 8 / 32 / 128 sweep, the M=3072 prefill
+layer (192 experts, K in {3,4}, Zipf-skewed routing), the roofline of the
+dominant kernel, an end-to-end figure through the C ABI with host buffers and
+the float64 CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica
+(the layer has no exchange step on one GPU); value = tokens of all ranks /
+max over ranks of the timed-region time.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s and HBM GB/s (% roofline) per EXL3 MoE layer at M=1 and M=3072"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _src_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "trellis_quantized_moe_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if the sources match."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("src_hash") == _src_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        return dist, dist.get_rank(), int(os.environ.get("LOCAL_RANK", "0")), ws
+    return None, 0, 0, 1
+
+
+def _max_over_ranks(dist, v):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _layer_bytes(w, ids):
+    """Algorithmic HBM bytes of one layer call: trellis words of the touched
+    experts, their fp16 rotation/scale vectors, activations in and out."""
+    s = w.spec
+    act = 2
+    active = np.unique(ids)
+    trellis = sum(3 * s.hidden * s.inter * int(s.K[e]) // 8 for e in active)
+    vectors = len(active) * (4 * s.hidden + 5 * s.inter) * 2
+    io = s.M * s.hidden * act * 2 + ids.size * (4 if s.ids_dtype == "i32" else 8) + ids.size * 2
+    return trellis + vectors + io
+
+
+def _gateup_bytes(w, ids):
+    """Algorithmic bytes of the gate/up kernel: gate+up trellis of the touched
+    experts, their vectors, rotated fp16 inputs in, fp16 down inputs out."""
+    s = w.spec
+    active = np.unique(ids)
+    R = ids.size
+    trellis = sum(2 * s.hidden * s.inter * int(s.K[e]) // 8 for e in active)
+    vectors = len(active) * (2 * (s.hidden + 2 * s.inter) + s.inter) * 2
+    return trellis + vectors + R * 2 * s.hidden * 2 + R * s.inter * 2
+
+
+def run_reference(args):
+    """The float64 oracle on the host cores, each step one bounded sample."""
+    from oracle import exl3_oracle as O
+    from workloads import MoEWorkload, act_to_f64, config, rw_to_f64
+    w = MoEWorkload(config(1, M=1))
+    s = w.spec
+    x, rw = act_to_f64(w.x, s.act), rw_to_f64(w.rw, s.rw_dtype)
+
+    def step():
+        O.moe_forward(x, w.ids, rw, w.projection)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * s.M / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded uniform trellis words, N(0,1) activations, softmax top-8 routing)",
+        "config": {"workload": "decode-shaped EXL3 MoE layer, hidden 5120, inter 1536, 192 experts,"
+                               " top-8, K=3 mcg, M=1", "M": 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.oracle_threads(), "kind": "oracle",
+                         "sample": "one M=1 layer call (8 experts decoded) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def cpu_baseline(budget_s=12.0):
+    """Oracle tokens/s on the host cores: repeated M=1 decode-layer calls."""
+    from oracle import exl3_oracle as O
+    from workloads import MoEWorkload, act_to_f64, config, rw_to_f64
+    n, t_used = 0, 0.0
+    t_start = time.perf_counter()
+    while t_used < budget_s and n < 6:
+        w = MoEWorkload(config(1, M=1))
+        s = w.spec
+        x, rw = act_to_f64(w.x, s.act), rw_to_f64(w.rw, s.rw_dtype)
+        t0 = time.perf_counter()
+        O.moe_forward(x, w.ids, rw, w.projection)
+        t_used += time.perf_counter() - t0
+        n += 1
+        if time.perf_counter() - t_start > 3 * budget_s:
+            break
+    return {"value": n / t_used, "unit": UNIT, "cores": O.oracle_threads(), "kind": "oracle",
+            "sample": f"{n} M=1 decode-layer calls (8 experts each, float64, C decode + numpy)"}
+
+
+def run_ours(args):
+    import torch
+    dist, rank, local_rank, world = _dist()
+    torch.cuda.set_device(local_rank)
+    import trellis_quantized_moe_gb300 as X
+    from workloads import MoEWorkload, config
+
+    hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
+    dev = torch.device("cuda", local_rank)
+
+    def dev_inputs(w):
+        s = w.spec
+        x = torch.from_numpy(w.x.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        ids = torch.from_numpy(w.ids).to(dev)
+        rw = torch.from_numpy(w.rw.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        out = torch.empty((s.M, s.hidden), dtype=torch.bfloat16, device=dev)
+        return x, ids, rw, out
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(call, steps, warmup, profile=False):
+        """Per-step device time (ms) with an L2 flush before each step."""
+        for _ in range(warmup):
+            flush.fill_(1)
+            call()
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        profs = [X.binding.ProfileEvents() for _ in range(steps)] if profile else None
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record()
+            if profile:
+                with profs[i]:
+                    call()
+            else:
+                call()
+            ends[i].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if dist is not None:
+            dist.barrier()
+        ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        kern = np.array([p.times_ms() for p in profs]) if profile else None
+        return ms, kern, wall
+
+    # ---------------- decode-shaped layer (headline M=1 and the M sweep)
+    base = MoEWorkload(config(1, M=1))
+    ex = X.DeviceExperts.from_workload(base)
+    spec = base.spec
+    Ms = [1, 8, 32, 128]
+    wls = {M: MoEWorkload(config(1, M=M)) for M in Ms}
+    ws = torch.empty(X.exl3_moe_workspace_bytes(128, 8, spec.E, spec.hidden, spec.inter,
+                                                spec.capacity), dtype=torch.uint8, device=dev)
+    inputs = {M: dev_inputs(wls[M]) for M in Ms}
+
+    def layer(M):
+        x, ids, rw, out = inputs[M]
+        return lambda: X.exl3_moe_forward(x, ids, rw, ex, spec.capacity, ws, out)
+
+    with Clocks(local_rank) as clk:
+        ms, kern, wall = timed(layer(1), args.steps, args.warmup, profile=True)
+    clocks = clk.summary()
+    assert X.exl3_workspace_error(ws) == 0
+    t_step = float(np.mean(ms))
+    t_step_max = _max_over_ranks(dist, t_step)
+    value = world * 1 / (t_step_max * 1e-3)
+    kmean = kern.mean(axis=0)
+    w1 = wls[1]
+    layer_bytes = _layer_bytes(w1, w1.ids)
+    gu_bytes = _gateup_bytes(w1, w1.ids)
+    gu_ms = float(kmean[2])
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+
+    sweep = {}
+    for M in Ms[1:]:
+        m_ms, m_kern, _ = timed(layer(M), max(5, args.steps // 4), 2, profile=True)
+        tm = float(np.mean(m_ms))
+        b = _layer_bytes(wls[M], wls[M].ids)
+        sweep[f"M={M}"] = {"us": 1e3 * tm, "tokens_per_s": M / (tm * 1e-3),
+                           "layer_gbs": b / (tm * 1e-3) / 1e9,
+                           "layer_frac_hbm": b / (tm * 1e-3) / 1e9 / hbm_peak,
+                           "kernel_us": [1e3 * float(v) for v in m_kern.mean(axis=0)]}
+
+    # ---------------- end to end through the C ABI with host buffers (M=1)
+    x_d, ids_d, rw_d, out_d = inputs[1]
+    x_h = x_d.cpu().pin_memory()
+    ids_h = ids_d.cpu().pin_memory()
+    rw_h = rw_d.cpu().pin_memory()
+    out_h = torch.empty_like(out_d, device="cpu").pin_memory()
+
+    def e2e_call():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        rw_d.copy_(rw_h, non_blocking=True)
+        X.exl3_moe_forward(x_d, ids_d, rw_d, ex, spec.capacity, ws, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+
+    e_ms, _, _ = timed(e2e_call, args.steps, args.warmup)
+    e_t = _max_over_ranks(dist, float(np.mean(e_ms)))
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + rw_h.numel() * 2
+    d2h = out_h.numel() * 2
+
+    # ---------------- prefill layer, M = 3072
+    del ex
+    torch.cuda.empty_cache()
+    pw = MoEWorkload(config(3))
+    ps = pw.spec
+    pex = X.DeviceExperts.from_workload(pw)
+    pws = torch.empty(X.exl3_moe_workspace_bytes(ps.M, ps.topk, ps.E, ps.hidden, ps.inter,
+                                                 ps.capacity), dtype=torch.uint8, device=dev)
+    px, pids, prw, pout = dev_inputs(pw)
+    p_ms, p_kern, _ = timed(lambda: X.exl3_moe_forward(px, pids, prw, pex, ps.capacity, pws, pout),
+                            max(3, min(10, args.steps // 5)), 1, profile=True)
+    assert X.exl3_workspace_error(pws) == 0
+    pt = float(np.mean(p_ms))
+    flops = 2.0 * ps.M * ps.topk * 3 * ps.hidden * ps.inter
+    prefill = {"workload": "hidden 5120, inter 1536, 192 experts, top-8, M=3072, K in {3,4} mcg, "
+                           "Zipf(1.2) expert bias, capacity 512, bf16",
+               "us": 1e3 * pt, "tokens_per_s": ps.M / (pt * 1e-3),
+               "tflops_dense_equiv": flops / (pt * 1e-3) / 1e12,
+               "frac_of_fp16_peak": flops / (pt * 1e-3) / 1e12 / bf16_peak,
+               "peak_tflops": bf16_peak, "peak_note": f"bf16 burst ({peak_src}) x 1.0 fp16:bf16",
+               "layer_gbs": _layer_bytes(pw, pw.ids) / (pt * 1e-3) / 1e9,
+               "kernel_us": [1e3 * float(v) for v in p_kern.mean(axis=0)]}
+    del pex, pws
+    torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded uniform trellis words, N(0,1) activations, softmax top-8 routing)",
+        "config": {"workload": "decode-shaped EXL3 MoE layer: hidden 5120, inter 1536, 192 experts,"
+                               " top-8, M=1, K=3 mcg, bf16 in/out, f16 MMA operands, f32 accumulate",
+                   "M": 1, "l2": "flushed before every timed step (256 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "layer_gbs": layer_bytes / (t_step_max * 1e-3) / 1e9,
+        "layer_frac_hbm": layer_bytes / (t_step_max * 1e-3) / 1e9 / hbm_peak,
+        "kernel_us": dict(zip(["route_pack", "rotate", "gate_up", "down_combine"],
+                              [1e3 * float(v) for v in kmean])),
+        "roofline": {"kernel": "k_expert_gemm<gate/up>", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": _traffic("gate_up_m1"), "algorithmic_bytes": gu_bytes,
+                     "peak_source": peak_src},
+        "sweep": sweep,
+        "prefill_m3072": prefill,
+        "e2e": {"value": world * 1 / (e_t * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

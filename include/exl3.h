@@ -148,7 +148,8 @@ int exl3_route_pack_max_tiles(int M, int topk, int E, int capacity);
 
 /* Route histogram, exclusive scan and stable packing (exllamav3 #284,
  * "Summary" and "Relationship to #246").
- *   ids: [M][topk] int32 or int64 (ids_dtype), expert of flat route f = t*topk + j.
+ *   ids: [M][topk] int32 or int64 (ids_dtype), expert of flat route f = t*topk + j
+ *        (ids, packed and tiles may be NULL when M == 0).
  *   offsets: int32 [E+1], offsets[e] = first packed slot of expert e.
  *   packed:  int32 [M*topk], packed[offsets[e] + r] = the r-th smallest f with
  *            id e (stable in f; bit-exact).
@@ -194,6 +195,15 @@ int exl3_moe_additive(const void *x, int act_dtype, int M, int hidden, int inter
                       int topk, const void *ids, int ids_dtype, const void *rw, int rw_dtype,
                       const exl3_experts *experts, const exl3_stages *stages, int capacity,
                       void *workspace, size_t ws_bytes, void *out, cudaStream_t stream);
+
+/* Benchmark instrumentation: when `events` is non-NULL, the following calls of
+ * exl3_moe_forward / exl3_moe_additive on this host thread record the five
+ * cudaEvent_t in events[0..4] on their stream before the route pack, after the
+ * route pack, after the input rotation, after the gate/up GEMM and after the
+ * down GEMM + combine, so that each kernel's time can be read with
+ * cudaEventElapsedTime.  NULL switches recording off.  The events stay owned
+ * by the caller.  Always returns EXL3_OK. */
+int exl3_profile_events(void *const *events);
 
 /* Reads the device error word of the last call that used `workspace`.
  * SYNCHRONISES `stream`; for tests and debugging, never inside a capture. */

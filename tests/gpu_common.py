@@ -35,6 +35,25 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
     return r, m
 
 
+def ulp(ref: np.ndarray, act: str) -> np.ndarray:
+    """One unit in the last place of the output dtype at |ref|."""
+    mant = 7 if act == "bf16" else 10
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-30)))
+    return np.exp2(e - mant)
+
+
+def assert_close_linear(got: np.ndarray, ref: np.ndarray, act: str, what: str = ""):
+    """Single projection (outputs O(1), unlike the layer's O(0.05)): rel-L2 2e-3
+    and a worst-element bound of one output ulp plus 1e-2 of the output RMS."""
+    assert got.shape == ref.shape and np.all(np.isfinite(got)), what
+    r = rel_l2(got, ref)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = np.abs(got - ref) - ulp(ref, act)
+    worst = float(np.max(excess)) / rms if got.size else 0.0
+    assert r <= REL_L2 and worst <= MAX_ABS, f"{what}: rel_l2={r:.3e} worst/rms={worst:.3e}"
+    return r, worst
+
+
 def moe_inputs(w):
     s = w.spec
     x = to_device(w.x, s.act)

@@ -17,7 +17,7 @@ import trellis_quantized_moe_gb300 as X  # noqa: E402
 from oracle import exl3_oracle as O  # noqa: E402
 from workloads import (CB_3INST, CB_MCG, CB_MUL1, LinearWorkload, MoEWorkload,  # noqa: E402
                        act_to_f64, config)
-from gpu_common import (assert_close, moe_inputs, oracle_rows, out_tensor, to_device,  # noqa: E402
+from gpu_common import (assert_close, assert_close_linear, moe_inputs, oracle_rows, out_tensor, to_device,  # noqa: E402
                         to_f64)
 
 
@@ -94,7 +94,7 @@ def test_linear_every_width_and_codebook(K, cb):
     lw = LinearWorkload(M=5, in_f=640, out_f=384, K=K, cb=cb, act="f16", seed=K * 3 + cb)
     y = to_f64(_linear_gpu(lw))
     ref = O.linear(act_to_f64(lw.x, "f16"), lw.proj)
-    assert_close(y, ref, f"linear K={K} cb={cb}")
+    assert_close_linear(y, ref, "f16", f"linear K={K} cb={cb}")
 
 
 @pytest.mark.parametrize("M,in_f,out_f,act", [(1, 4096, 1408, "bf16"), (37, 1408, 4096, "f16"),
@@ -104,7 +104,7 @@ def test_linear_shapes(M, in_f, out_f, act):
     y = to_f64(_linear_gpu(lw))
     rows = np.arange(min(M, 24))
     ref = O.linear(act_to_f64(lw.x, act)[rows], lw.proj)
-    assert_close(y[rows], ref, f"linear {M}x{in_f}x{out_f}")
+    assert_close_linear(y[rows], ref, act, f"linear {M}x{in_f}x{out_f}")
 
 
 def test_linear_rows_are_byte_invariant_across_row_counts():

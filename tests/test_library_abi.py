@@ -18,8 +18,10 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from trellis_quantized_moe_gb300.build import build
-    return ctypes.CDLL(build())
+    import __graft_entry__
+    __graft_entry__.build()
+    return ctypes.CDLL(os.path.join(ROOT, "trellis_quantized_moe_gb300", "_lib",
+                                    "libexl3_gb300.so"))
 
 
 def test_every_declared_symbol_is_exported(lib):

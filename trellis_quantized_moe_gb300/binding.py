@@ -71,6 +71,8 @@ def _load():
     lib.exl3_moe_additive.argtypes = [V, I, I, I, I, I, I, V, I, V, I, P(exl3_experts),
                                       P(exl3_stages), I, V, Z, V, V]
     lib.exl3_moe_additive.restype = I
+    lib.exl3_profile_events.argtypes = [V]
+    lib.exl3_profile_events.restype = I
     lib.exl3_workspace_error.argtypes = [V, P(ctypes.c_int32), V]
     lib.exl3_workspace_error.restype = I
     return lib
@@ -79,7 +81,7 @@ def _load():
 _lib = _load()
 EXPORTED = ["exl3_abi_version", "exl3_moe_workspace_bytes", "exl3_linear_workspace_bytes",
             "exl3_route_pack_max_tiles", "exl3_route_pack", "exl3_linear", "exl3_moe_forward",
-            "exl3_moe_additive", "exl3_workspace_error"]
+            "exl3_moe_additive", "exl3_profile_events", "exl3_workspace_error"]
 
 
 def lib():
@@ -273,6 +275,30 @@ def exl3_moe_additive(x, ids, rw, experts: DeviceExperts, stages: DeviceStages, 
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _ptr(out), _stream(stream))
     return _check("exl3_moe_additive", rc, raise_on_error)
+
+
+class ProfileEvents:
+    """Five torch CUDA events recorded between the fused layer's kernels
+    (route pack | rotation | gate/up GEMM | down GEMM + combine)."""
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in self.events:          # creates the underlying cudaEvent_t
+            e.record()
+        torch.cuda.synchronize()
+        self._arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
+
+    def __enter__(self):
+        _lib.exl3_profile_events(ctypes.cast(self._arr, ctypes.c_void_p))
+        return self
+
+    def __exit__(self, *exc):
+        _lib.exl3_profile_events(None)
+
+    def times_ms(self):
+        """(route pack, rotation, gate/up, down + combine) in ms for the last call."""
+        e = self.events
+        return [e[i].elapsed_time(e[i + 1]) for i in range(4)]
 
 
 def exl3_workspace_error(workspace, stream=None) -> int:

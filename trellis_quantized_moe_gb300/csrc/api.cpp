@@ -20,6 +20,13 @@ struct DeviceState {
 
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+thread_local void *const *g_prof_events = nullptr;
+
+void prof_mark(int i, cudaStream_t s)
+{
+    if (g_prof_events)
+        cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[i]), s);
+}
 
 // Device of the stream (must be the current device); lazily sets kernel attributes.
 int setup_device(cudaStream_t s, int *dev_out, int *sms_out)
@@ -140,8 +147,10 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.s_trellis = additive ? st->trellis : nullptr;
     rp.s_scale = additive ? st->scale : nullptr;
     rp.s_K = additive ? st->K : nullptr;
+    prof_mark(0, s);
     if (launch_route_pack(rp, ids_dtype, s) != cudaSuccess)
         return EXL3_E_CUDA;
+    prof_mark(1, s);
 
     RotateArgs ra{};
     ra.x = x;
@@ -160,6 +169,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     ra.nzero = (int)((L.cnt2 - L.cnt) / 4) + L.split_pairs2;
     if (launch_rotate(ra, s) != cudaSuccess)
         return EXL3_E_CUDA;
+    prof_mark(2, s);
 
     GemmArgs g{};
     g.act_dtype = act_dtype;
@@ -191,6 +201,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
     if (launch_gemm_gateup(additive, nrb, g, sms * ctas, s) != cudaSuccess)
         return EXL3_E_CUDA;
+    prof_mark(3, s);
 
     // down: [R][inter] -> [R][hidden] fp32 staging -> combine into out
     g.in_f = inter;
@@ -209,6 +220,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.out = out;
     if (launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess)
         return EXL3_E_CUDA;
+    prof_mark(4, s);
     return EXL3_OK;
 }
 
@@ -247,7 +259,7 @@ int exl3_route_pack(const void *ids, int ids_dtype, int M, int topk, int E, int 
                     cudaStream_t stream)
 {
     int dev, sms;
-    if (!ids || !offsets || !info || (M > 0 && (!packed || !tiles)))
+    if (!offsets || !info || (M > 0 && (!ids || !packed || !tiles)))
         return EXL3_E_NULL;
     if (!ids_dtype_ok(ids_dtype))
         return EXL3_E_DTYPE;
@@ -263,8 +275,10 @@ int exl3_route_pack(const void *ids, int ids_dtype, int M, int topk, int E, int 
         return rc;
     const void *ptrs[] = {ids, offsets, info, packed, tiles};
     for (const void *p : ptrs)
-        if (p && !on_device(p, dev))
+        if (p && M > 0 && !on_device(p, dev))
             return EXL3_E_DEVICE;
+    if (!on_device(offsets, dev) || !on_device(info, dev))
+        return EXL3_E_DEVICE;
     RoutePackArgs rp{};
     rp.ids = ids;
     rp.R = M * topk;
@@ -394,6 +408,12 @@ int exl3_moe_additive(const void *x, int act_dtype, int M, int hidden, int inter
         return rc;
     return run_moe(x, act_dtype, M, hidden, inter, E, topk, ids, ids_dtype, rw, rw_dtype, ex, st,
                    capacity, ws, out, sms, stream);
+}
+
+int exl3_profile_events(void *const *events)
+{
+    g_prof_events = events;
+    return EXL3_OK;
 }
 
 int exl3_workspace_error(const void *ws, int32_t *err_host, cudaStream_t stream)
