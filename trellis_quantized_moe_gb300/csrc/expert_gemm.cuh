@@ -167,17 +167,20 @@ __device__ __forceinline__ void producer_init(const GemmArgs &a, Producer &P, in
     }
 }
 
+__host__ __device__ constexpr int rows_per_slot(int K) { return kSlotBytes / (256 * K); }
+
 template <int MODE, int NRB, bool ADD>
 __device__ __forceinline__ bool producer_next(const GemmArgs &a, Producer &P, int warp,
-                                              const uint32_t **src, uint32_t *bytes)
+                                              const uint32_t **src, int *nrows, int *K)
 {
     const int npass = ADD ? a.num_stages : 1;
     while (!P.done) {
         if (P.have && P.tk < P.ps.tk1) {
             *src = P.ps.trellis +
                    ((size_t)P.tk * (a.out_f / 16) + (size_t)P.it.nbk * 8) * (8 * P.ps.K);
-            *bytes = 256u * P.ps.K;
-            P.tk++;
+            *K = P.ps.K;
+            *nrows = min(rows_per_slot(P.ps.K), P.ps.tk1 - P.tk);
+            P.tk += *nrows;
             return true;
         }
         P.have = false;
@@ -225,13 +228,19 @@ __device__ __forceinline__ void ring_issue(Ring &r, const GemmArgs &a, int warp)
         return;
     WarpStream *w = r.ws;
     const uint32_t *src;
-    uint32_t bytes;
+    int nrows, K;
     if (w->dead)
         return;
-    if (producer_next<MODE, NRB, ADD>(a, w->P, warp, &src, &bytes)) {
+    if (producer_next<MODE, NRB, ADD>(a, w->P, warp, &src, &nrows, &K)) {
+        // one slot = nrows consecutive tk rows of the 8 tiles of the block,
+        // one bulk copy each, all completing on the slot's mbarrier
         const int slot = w->issued % kSlots;
-        mbar_arrive_expect_tx(&r.bar[slot], bytes);
-        bulk_g2s(r.buf + slot * kSlotBytes, src, bytes, &r.bar[slot]);
+        const uint32_t row_bytes = 256u * K;
+        const size_t row_stride = (size_t)(a.out_f / 16) * 8 * K;   // words between tk rows
+        mbar_arrive_expect_tx(&r.bar[slot], row_bytes * nrows);
+        for (int i = 0; i < nrows; i++)
+            bulk_g2s(r.buf + slot * kSlotBytes + i * row_bytes, src + i * row_stride, row_bytes,
+                     &r.bar[slot]);
         w->issued++;
     }
 }
@@ -299,10 +308,14 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
     const uint32_t mul = MUL1 ? 0x83DCD12Du : (ps.cb == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
     const uint32_t add = (!MUL1 && ps.cb == EXL3_CB_3INST) ? 64248484u : 0u;
 
-    for (int tk = ps.tk0; tk < ps.tk1; tk++) {
+    constexpr int RPS = rows_per_slot(K);
+    for (int tk_s = ps.tk0; tk_s < ps.tk1; tk_s += RPS) {
+        const int nrows = min(RPS, ps.tk1 - tk_s);
         const uint32_t *seg = ring_wait(ring, a.hdr);
-        if (seg != nullptr) {
-            const uint32_t seg_s = smem_addr(seg);
+#pragma unroll 1
+        for (int rr = 0; rr < nrows && seg != nullptr; rr++) {
+            const int tk = tk_s + rr;
+            const uint32_t seg_s = smem_addr(seg) + rr * 256 * K;
             const int kcol = (tk - chunk * kChunkTk) * 16 + 4 * t;
             uint32_t bf[NRB][4];
 #pragma unroll
@@ -614,16 +627,24 @@ __global__ void __launch_bounds__(kThreads, NRB == 1 ? 2 : 1) k_expert_gemm(Gemm
                 continue;
             __threadfence();
             const float *src = a.part + (size_t)it.pair * a.nchunks * T::nproj * kPartStride;
-            for (int e = tid; e < T::nproj * FRAG * 32; e += kThreads) {
-                const int off = (e / (FRAG * 32)) * kPartStride + e % (FRAG * 32);
-                float run = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < a.nchunks; c++) {
-                    const float v = __ldcg(src + (size_t)c * T::nproj * kPartStride + off);
-                    run = (c == 0) ? v : run + v;
+            constexpr int PER = T::nproj * FRAG * 32 / kThreads;   // elements per thread
+            float run[PER];
+#pragma unroll 2
+            for (int c = 0; c < a.nchunks; c++) {
+                const float *sc = src + (size_t)c * T::nproj * kPartStride;
+                float v[PER];
+#pragma unroll
+                for (int k = 0; k < PER; k++) {
+                    const int e = tid + k * kThreads;
+                    v[k] = __ldcg(sc + (e / (FRAG * 32)) * kPartStride + e % (FRAG * 32));
                 }
-                zs[zs_index<ROWS>(e, FRAG)] = run;
+#pragma unroll
+                for (int k = 0; k < PER; k++)
+                    run[k] = (c == 0) ? v[k] : run[k] + v[k];
             }
+#pragma unroll
+            for (int k = 0; k < PER; k++)
+                zs[zs_index<ROWS>(tid + k * kThreads, FRAG)] = run[k];
             if (tid == 0)
                 a.cnt_split[it.pair] = 0;
         }

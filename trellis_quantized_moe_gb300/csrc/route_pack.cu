@@ -189,21 +189,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
 
     // the fused layer: validate the tables of every expert that receives routes
     if (a.plan && tid < E && cnt > 0) {
-        bool bad = false;
-        for (int p = 0; p < 3; p++) {
+        int K[3], cb[3];
+        long long tr[3], su[3], sv[3], sc[3];
+#pragma unroll
+        for (int p = 0; p < 3; p++) {          // independent loads, issued together
             const int i = tid * 3 + p;
-            const int K = a.t_K[i], cb = a.t_cb[i];
-            const long long tr = a.t_trellis[i];
-            bad |= K < 1 || K > 8 || cb < 0 || cb > 2 || tr == 0 || (tr & 15);
-            bad |= a.t_suh[i] == 0 || (a.t_suh[i] & 7) || a.t_svh[i] == 0 || (a.t_svh[i] & 7) ||
-                   a.t_scale[i] == 0 || (a.t_scale[i] & 7);
-            for (int s = 1; s < a.num_stages; s++) {
+            K[p] = a.t_K[i];
+            cb[p] = a.t_cb[i];
+            tr[p] = a.t_trellis[i];
+            su[p] = a.t_suh[i];
+            sv[p] = a.t_svh[i];
+            sc[p] = a.t_scale[i];
+        }
+        bool bad = false;
+#pragma unroll
+        for (int p = 0; p < 3; p++) {
+            bad |= (K[p] < 1) | (K[p] > 8) | (cb[p] < 0) | (cb[p] > 2) | (tr[p] == 0) |
+                   ((tr[p] & 15) != 0) | (su[p] == 0) | ((su[p] & 7) != 0) | (sv[p] == 0) |
+                   ((sv[p] & 7) != 0) | (sc[p] == 0) | ((sc[p] & 7) != 0);
+        }
+        for (int s = 1; s < a.num_stages; s++) {
+#pragma unroll
+            for (int p = 0; p < 3; p++) {
                 const int j = ((s - 1) * E + tid) * 3 + p;
-                if (a.s_scale[j] != 0.0f) {
-                    const int Ks = a.s_K[j];
-                    const long long ts = a.s_trellis[j];
-                    bad |= Ks < 1 || Ks > 8 || ts == 0 || (ts & 15);
-                }
+                const float al = a.s_scale[j];
+                const int Ks = a.s_K[j];
+                const long long ts = a.s_trellis[j];
+                if (al != 0.0f)
+                    bad |= (Ks < 1) | (Ks > 8) | (ts == 0) | ((ts & 15) != 0);
             }
         }
         if (bad)
