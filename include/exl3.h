@@ -196,6 +196,22 @@ int exl3_moe_additive(const void *x, int act_dtype, int M, int hidden, int inter
                       const exl3_experts *experts, const exl3_stages *stages, int capacity,
                       void *workspace, size_t ws_bytes, void *out, cudaStream_t stream);
 
+/* exl3_linear for callers that cannot allocate device memory (graph replays
+ * without a memory pool, hosts whose allocator forbids cudaMalloc, paths where
+ * an allocation would synchronise).  Same result as exl3_linear, but its
+ * workspace is one fixed scratch array inside the library's device image
+ * (exl3_linear_noalloc_max_scratch_bytes() bytes, resident on every GPU that
+ * loads the library until the process exits).  Allocates nothing.  The first
+ * call on a device looks up the scratch address for that device (make it
+ * before any stream capture).  Calls whose exl3_linear_workspace_bytes(M, in,
+ * out) exceeds the scratch size return EXL3_E_WORKSPACE without launching.
+ * All calls share the scratch: calls that may overlap on the GPU (different
+ * streams, or graphs replayed concurrently) race and must be serialised by the
+ * caller.  The pages have no counterpart; this entry point is an addition. */
+size_t exl3_linear_noalloc_max_scratch_bytes(void);
+int exl3_linear_noalloc(const void *x, int act_dtype, int M, const exl3_proj *proj, void *y,
+                        cudaStream_t stream);
+
 /* Benchmark instrumentation: when `events` is non-NULL, the following calls of
  * exl3_moe_forward / exl3_moe_additive on this host thread record the five
  * cudaEvent_t in events[0..4] on their stream before the route pack, after the
