@@ -186,6 +186,36 @@ def test_decode_layer_rows_byte_invariant_across_batch_sizes():
         assert np.array_equal(o[:1], ref[:1]), M
 
 
+def _small_layer(M, act, seed, E=8, topk=2):
+    from workloads import MoESpec
+    Ks = [1, 2, 3, 4, 5, 6, 7, 8][:E]
+    cbs = [CB_MCG, CB_3INST, CB_MUL1, CB_MCG, CB_3INST, CB_MUL1, CB_MCG, CB_3INST][:E]
+    spec = MoESpec("small", 512, 256, E, topk, M, act, "i32", "f16", np.array(Ks), np.array(cbs),
+                   seed=seed)
+    return MoEWorkload(spec)
+
+
+@pytest.mark.parametrize("M,act", [(512, "f16"), (1100, "bf16")])
+def test_prefill_path_small_layer_full_parity(M, act):
+    # M > 128 with > 64 routes per expert: the tcgen05 path; M=1100 puts more
+    # than 256 routes on some experts (several row tiles per expert)
+    w = _small_layer(M, act, seed=40 + M)
+    ex = X.DeviceExperts.from_workload(w)
+    assert np.bincount(w.ids.reshape(-1), minlength=8).max() > (256 if M > 1000 else 64)
+    out = to_f64(run_layer(w, ex))
+    # outputs are O(1) here (8 experts, top-2): worst element within one output
+    # ulp plus 1e-2 of the output rms, rel-L2 2e-3
+    assert_close_linear(out, oracle_rows(w), act, f"prefill path M={M}")
+
+
+def test_prefill_path_rows_do_not_depend_on_capacity():
+    w = _small_layer(600, "f16", seed=7)
+    ex = X.DeviceExperts.from_workload(w)
+    a = run_layer(w, ex, capacity=512).view(torch.int16).cpu().numpy()
+    b = run_layer(w, ex, capacity=97).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
 def test_mixed_width_layer_parity():
     w = MoEWorkload(config(2))
     out = to_f64(run_layer(w, _experts(2)))

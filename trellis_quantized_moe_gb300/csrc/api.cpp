@@ -46,7 +46,8 @@ int setup_device(cudaStream_t s, int *dev_out, int *sms_out)
         if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return EXL3_E_CUDA;
         if (route_pack_set_attributes() != cudaSuccess || gemm_gateup_set_attributes() != cudaSuccess ||
-            gemm_down_set_attributes() != cudaSuccess || gemm_linear_set_attributes() != cudaSuccess)
+            gemm_down_set_attributes() != cudaSuccess || gemm_linear_set_attributes() != cudaSuccess ||
+            tc_set_attributes() != cudaSuccess)
             return EXL3_E_CUDA;
         d.ready = true;
     }
@@ -112,17 +113,22 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     uint8_t *w = static_cast<uint8_t *>(ws);
     int32_t *hdr = reinterpret_cast<int32_t *>(w + L.hdr);
     const int R = L.R;
-    // 16-row items (1 CTA/SM) when experts carry many routes on average, else 8 rows
+    // Prefill regime (tcgen05, up to 256 routes per item): more than 128 tokens,
+    // no residual stages and spans of more than 64 routes per expert on
+    // average.  Otherwise the decode regime (mma.sync): 16-row items (1 CTA/SM)
+    // when experts carry more than 8 routes on average, else 8 rows.  M <= 128
+    // always takes the decode regime, so a row's bytes never depend on M there.
     const int active = E < R ? E : R;
+    const bool use_tc = !additive && M > 128 && (long long)R > 64LL * active;
     const int nrb = additive ? 1 : (R > 8 * active ? 2 : 1);
-    const int ctas = nrb == 2 ? kGemmCtasPerSm16 : kGemmCtasPerSm8;
+    const int ctas = gemm_ctas_per_sm(nrb, additive);
 
     RoutePackArgs rp{};
     rp.ids = ids;
     rp.R = R;
     rp.E = E;
     rp.capacity = capacity;
-    rp.rg_size = 8 * nrb;
+    rp.rg_size = use_tc ? tc_rows_per_item() : 8 * nrb;
     rp.nw = route_pack_hist_warps(E);
     rp.offsets = reinterpret_cast<int32_t *>(w + L.offsets);
     rp.packed = reinterpret_cast<int32_t *>(w + L.packed);
@@ -132,8 +138,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.rg = w + L.rg;
     rp.nb1 = L.nb1;
     rp.nb2 = L.nb2;
-    rp.nchunks1 = L.nchunks1;
-    rp.nchunks2 = L.nchunks2;
+    rp.nchunks1 = use_tc ? 1 : L.nchunks1;     // the prefill path never splits chunks
+    rp.nchunks2 = use_tc ? 1 : L.nchunks2;
     rp.split_pairs1 = L.split_pairs1;
     rp.split_pairs2 = L.split_pairs2;
     rp.num_sms = sms;
@@ -199,7 +205,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.part = reinterpret_cast<float *>(w + L.part1);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
-    if (launch_gemm_gateup(additive, nrb, g, sms * ctas, s) != cudaSuccess)
+    if ((use_tc ? launch_tc_gateup(g, sms, s) : launch_gemm_gateup(additive, nrb, g, sms * ctas, s)) !=
+        cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(3, s);
 
@@ -218,7 +225,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.rw_dtype = rw_dtype;
     g.cnt_comb = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = out;
-    if (launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess)
+    if ((use_tc ? launch_tc_down(g, sms, s) : launch_gemm_down(additive, nrb, g, sms * ctas, s)) !=
+        cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(4, s);
     return EXL3_OK;
@@ -358,7 +366,7 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
     g.part = reinterpret_cast<float *>(w + L.part);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = y;
-    int grid = sms * kGemmCtasPerSm16;
+    int grid = sms * gemm_ctas_per_sm(2, false);
     if (grid > g.n_items_host)
         grid = g.n_items_host;
     return launch_gemm_linear(g, grid, stream) == cudaSuccess ? EXL3_OK : EXL3_E_CUDA;

@@ -164,8 +164,8 @@ EXL3_DEV void named_barrier(int id, int nthreads)
 EXL3_DEV void mma_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                         uint32_t b0, uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    // not volatile: the scheduler may interleave it with the next tile's loads
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -175,6 +175,25 @@ EXL3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// x >> 16 as the high word of x * 2^16 (runs on the FMA pipe, not the ALU pipe)
+EXL3_DEV uint32_t hi16_fma(uint32_t x)
+{
+    uint32_t d;
+    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// x << n for a compile-time n, as a funnel shift (ALU pipe)
+template <int N>
+EXL3_DEV uint32_t shl_alu(uint32_t x)
+{
+    if (N == 0)
+        return x;
+    uint32_t d;
+    asm("shf.l.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(0u), "r"(x), "n"(N));
     return d;
 }
 

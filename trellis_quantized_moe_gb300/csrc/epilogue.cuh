@@ -1,0 +1,106 @@
+// Per-row epilogues shared by the decode-regime (mma.sync) and prefill-regime
+// (tcgen05) grouped GEMMs.  One warp handles one route row of one 128-output
+// block; lane l owns outputs 4l..4l+3.  Inputs are the raw fp32 contraction
+// results z (before the output Hadamard).
+//
+// "EXL3 linear and grouped routed experts" (TensorFold #837), "What this
+// changes": output rotation, SwiGLU, down-input rotation, weighted combine.
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+
+namespace exl3 {
+
+// gate/up: g' = Hb(g)*svh*scale, u' likewise, h = silu(g')*u', then the down
+// projection's input rotation a_d = Hb(h * suh_down) over the same 128 block of
+// the intermediate dimension; stored as the fp16 MMA operand of the down GEMM.
+__device__ __forceinline__ void epi_gateup_row(const GemmArgs &a, int e, int nbk, int prow,
+                                               float gv[4], float uv[4])
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    float sv[4], sc[4], h[4];
+    warp_hadamard128(gv);
+    warp_hadamard128(uv);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 0]), col, sv);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 0]), col, sc);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        gv[i] = gv[i] * kInvSqrt128 * sv[i] * sc[i];
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 1]), col, sv);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 1]), col, sc);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        uv[i] = uv[i] * kInvSqrt128 * sv[i] * sc[i];
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + 2]), col, sv);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        h[i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i] * sv[i];
+    warp_hadamard128(h);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        h[i] *= kInvSqrt128;
+    store_act4(a.ad, (size_t)prow * a.out_f + col, EXL3_F16, h);
+}
+
+// down: d = Hb(z)*svh*scale into the fp32 staging row of flat route f; the
+// warp that completes all topk routes of a token's block combines them in j
+// order (fp32 fma chain, rounded once) and resets the block's counter.
+__device__ __forceinline__ void epi_down_row(const GemmArgs &a, int e, int nbk, int prow,
+                                             float z[4])
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    const uint16_t *svh = reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 2]);
+    const uint16_t *scl = reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 2]);
+    float sv[4], sc[4];
+    warp_hadamard128(z);
+    load_half4(svh, col, sv);
+    load_half4(scl, col, sc);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
+    const int f = a.packed[prow];
+    const int tok = f / a.topk;
+    *reinterpret_cast<float4 *>(a.stage + (size_t)f * a.out_f + col) =
+        make_float4(z[0], z[1], z[2], z[3]);
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if (lane == 0)
+        old = atomicAdd(&a.cnt_comb[tok * a.nb + nbk], 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == a.topk - 1) {
+        __threadfence();
+        float o4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < a.topk; j++) {
+            const float w = load_act(a.rw, (size_t)tok * a.topk + j, a.rw_dtype);
+            const float4 d = __ldcg(reinterpret_cast<const float4 *>(
+                a.stage + ((size_t)tok * a.topk + j) * a.out_f + col));
+            o4[0] = __fmaf_rn(w, d.x, o4[0]);
+            o4[1] = __fmaf_rn(w, d.y, o4[1]);
+            o4[2] = __fmaf_rn(w, d.z, o4[2]);
+            o4[3] = __fmaf_rn(w, d.w, o4[3]);
+        }
+        store_act4(a.out, (size_t)tok * a.out_f + col, a.act_dtype, o4);
+        if (lane == 0)
+            a.cnt_comb[tok * a.nb + nbk] = 0;
+    }
+}
+
+// linear: y = Hb(z)*svh*scale, stored in the activation dtype.
+__device__ __forceinline__ void epi_linear_row(const GemmArgs &a, int nbk, int row, float z[4])
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    float sv[4], sc[4];
+    warp_hadamard128(z);
+    load_half4(a.lin.svh, col, sv);
+    load_half4(a.lin.scale, col, sc);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
+    store_act4(a.out, (size_t)row * a.out_f + col, a.act_dtype, z);
+}
+
+}  // namespace exl3

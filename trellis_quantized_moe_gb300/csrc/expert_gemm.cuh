@@ -36,6 +36,7 @@
 // one CTA.  Both perform the same fp32 operations.
 #pragma once
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "kernels.h"
 
 namespace exl3 {
@@ -47,6 +48,9 @@ constexpr int kSlots = 3;
 constexpr int kSlotBytes = 2048;           // 8 tiles x 32*K bytes, K <= 8
 constexpr int kActLd = kChunk + 16;        // halves per activation row in smem
 constexpr int kZsLd = kHb + 4;             // floats per row of the z tile
+
+// resident CTAs per SM: 8-row items 3 (additive 2), 16-row items 1
+__host__ __device__ constexpr int ctas_per_sm(int nrb, bool add) { return nrb == 2 ? 1 : (add ? 2 : 3); }
 
 template <int MODE>
 struct ModeTraits {
@@ -145,10 +149,13 @@ __device__ __forceinline__ bool get_pass(const GemmArgs &a, const Item &it, int 
 // Enumerates, in consumption order, the trellis segments (one tk row of the 8
 // tiles of a 128-output block) that one warp streams.
 struct Producer {
-    int item, chunk, pass, tk, n_items;
-    bool split, have, done;
+    // fast path: rows left in the current (item, chunk, pass), next row, stride
+    const uint32_t *row;
+    int rows_left, rps, row_bytes, stride_words;
+    // slow path: position in the enumeration
+    int item, chunk, pass, n_items;
+    bool split, done;
     Item it;
-    Pass ps;
 };
 
 template <int MODE, int NRB, bool ADD>
@@ -158,7 +165,7 @@ __device__ __forceinline__ void producer_init(const GemmArgs &a, Producer &P, in
     P.n_items = n_items;
     P.split = split;
     P.item = blockIdx.x;
-    P.have = false;
+    P.rows_left = 0;
     P.done = P.item >= n_items;
     P.pass = -1;
     if (!P.done) {
@@ -171,22 +178,22 @@ __host__ __device__ constexpr int rows_per_slot(int K) { return kSlotBytes / (25
 
 template <int MODE, int NRB, bool ADD>
 __device__ __forceinline__ bool producer_next(const GemmArgs &a, Producer &P, int warp,
-                                              const uint32_t **src, int *nrows, int *K)
+                                              const uint32_t **src, int *nrows, int *row_bytes,
+                                              int *stride)
 {
     const int npass = ADD ? a.num_stages : 1;
-    while (!P.done) {
-        if (P.have && P.tk < P.ps.tk1) {
-            *src = P.ps.trellis +
-                   ((size_t)P.tk * (a.out_f / 16) + (size_t)P.it.nbk * 8) * (8 * P.ps.K);
-            *K = P.ps.K;
-            *nrows = min(rows_per_slot(P.ps.K), P.ps.tk1 - P.tk);
-            P.tk += *nrows;
-            return true;
-        }
-        P.have = false;
+    while (P.rows_left <= 0) {              // advance to the next pass with rows
+        if (P.done)
+            return false;
         if (++P.pass < npass) {
-            P.have = get_pass<MODE>(a, P.it, P.chunk, P.pass, warp, P.ps);
-            P.tk = P.ps.tk0;
+            Pass ps;
+            if (get_pass<MODE>(a, P.it, P.chunk, P.pass, warp, ps)) {
+                P.stride_words = (a.out_f / 16) * 8 * ps.K;
+                P.row = ps.trellis + (size_t)ps.tk0 * P.stride_words + (size_t)P.it.nbk * 64 * ps.K;
+                P.rows_left = ps.tk1 - ps.tk0;
+                P.rps = rows_per_slot(ps.K);
+                P.row_bytes = 256 * ps.K;
+            }
             continue;
         }
         P.pass = -1;
@@ -200,7 +207,15 @@ __device__ __forceinline__ bool producer_next(const GemmArgs &a, Producer &P, in
         load_item<MODE, NRB>(a, P.item, P.split, P.it);
         P.chunk = P.it.c_begin;
     }
-    return false;
+    // next slot of the current pass
+    const int n = min(P.rps, P.rows_left);
+    *src = P.row;
+    *nrows = n;
+    *row_bytes = P.row_bytes;
+    *stride = P.stride_words;
+    P.row += (size_t)n * P.stride_words;
+    P.rows_left -= n;
+    return true;
 }
 
 // Per-warp stream state.  The producer cursor lives in shared memory and only
@@ -228,19 +243,17 @@ __device__ __forceinline__ void ring_issue(Ring &r, const GemmArgs &a, int warp)
         return;
     WarpStream *w = r.ws;
     const uint32_t *src;
-    int nrows, K;
+    int nrows, row_bytes, stride;
     if (w->dead)
         return;
-    if (producer_next<MODE, NRB, ADD>(a, w->P, warp, &src, &nrows, &K)) {
+    if (producer_next<MODE, NRB, ADD>(a, w->P, warp, &src, &nrows, &row_bytes, &stride)) {
         // one slot = nrows consecutive tk rows of the 8 tiles of the block,
         // one bulk copy each, all completing on the slot's mbarrier
         const int slot = w->issued % kSlots;
-        const uint32_t row_bytes = 256u * K;
-        const size_t row_stride = (size_t)(a.out_f / 16) * 8 * K;   // words between tk rows
         mbar_arrive_expect_tx(&r.bar[slot], row_bytes * nrows);
         for (int i = 0; i < nrows; i++)
-            bulk_g2s(r.buf + slot * kSlotBytes + i * row_bytes, src + i * row_stride, row_bytes,
-                     &r.bar[slot]);
+            bulk_g2s(r.buf + slot * kSlotBytes + i * row_bytes, src + (size_t)i * stride,
+                     row_bytes, &r.bar[slot]);
         w->issued++;
     }
 }
@@ -292,21 +305,42 @@ __device__ __forceinline__ uint32_t hsub_1534(uint32_t v)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// State i (0..3) of a run whose 64-bit window X0:X1 starts at the run's first
+// window bit: bits [iK, iK+16).
+template <int K, int I>
+__device__ __forceinline__ uint32_t run_state(uint32_t X0, uint32_t X1)
+{
+    if (I * K + 16 <= 32)
+        return (X0 >> (16 - I * K)) & 0xFFFFu;
+    return __funnelshift_l(X1, X0, I * K) >> 16;
+}
+
+// codebook constants: x = a*s + b (mod 2^32)
+template <int CB>
+struct Codebook {
+    static constexpr uint32_t a = CB == EXL3_CB_MUL1 ? 0x83DCD12Du
+                                : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
+    static constexpr uint32_t b = CB == EXL3_CB_3INST ? 64248484u : 0u;
+};
+
 // Decode + MMA over the warp's tk slice of one (chunk, pass).
-template <int K, bool MUL1, int MODE, int NRB, bool ADD>
+template <int K, int CB, int MODE, int NRB, bool ADD>
 __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
                                          const GemmArgs &a, int warp, const Pass &ps,
                                          int chunk, const uint16_t *act_s)
 {
     constexpr int NWD = 8 * K;                // 32-bit words per tile
+    constexpr bool W3 = 16 + 3 * K > 33;      // a run's window needs a third word (K >= 6)
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int start = (16 * g + 4 * t + 1) * K - 16;   // first bit of run A's window
     const int w0 = start >> 5;                          // floor (may be -1)
     const int o = start & 31;
+    // word offsets (inside a tile) of the words of run A (column g) and run B
+    // (column g + 8, 128K bits later: same offset modulo 32)
     const int oA0 = (w0 + NWD) % NWD, oA1 = (w0 + 1 + NWD) % NWD, oA2 = (w0 + 2 + NWD) % NWD;
     const int oB0 = (w0 + 4 * K) % NWD, oB1 = (w0 + 4 * K + 1) % NWD, oB2 = (w0 + 4 * K + 2) % NWD;
-    const uint32_t mul = MUL1 ? 0x83DCD12Du : (ps.cb == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
-    const uint32_t add = (!MUL1 && ps.cb == EXL3_CB_3INST) ? 64248484u : 0u;
+    constexpr bool MUL1 = CB == EXL3_CB_MUL1;
+    constexpr uint32_t mul = Codebook<CB>::a, add = Codebook<CB>::b;
 
     constexpr int RPS = rows_per_slot(K);
     for (int tk_s = ps.tk0; tk_s < ps.tk1; tk_s += RPS) {
@@ -315,7 +349,7 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
 #pragma unroll 1
         for (int rr = 0; rr < nrows && seg != nullptr; rr++) {
             const int tk = tk_s + rr;
-            const uint32_t seg_s = smem_addr(seg) + rr * 256 * K;
+            const uint32_t *row = seg + rr * 64 * K;       // 8 tiles of 8K words
             const int kcol = (tk - chunk * kChunkTk) * 16 + 4 * t;
             uint32_t bf[NRB][4];
 #pragma unroll
@@ -334,19 +368,25 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
             }
 #pragma unroll
             for (int j = 0; j < 8; j++) {
-                const uint32_t tw = seg_s + j * NWD * 4;
-                const uint32_t a0 = lds_u32(tw + 4 * oA0), a1 = lds_u32(tw + 4 * oA1),
-                               a2 = lds_u32(tw + 4 * oA2);
-                const uint32_t b0 = lds_u32(tw + 4 * oB0), b1 = lds_u32(tw + 4 * oB1),
-                               b2 = lds_u32(tw + 4 * oB2);
-                const uint32_t XA0 = __funnelshift_l(a1, a0, o), XA1 = __funnelshift_l(a2, a1, o);
-                const uint32_t XB0 = __funnelshift_l(b1, b0, o), XB1 = __funnelshift_l(b2, b1, o);
-                uint32_t sA[4], sB[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    sA[i] = __funnelshift_l(XA1, XA0, i * K) >> 16;
-                    sB[i] = __funnelshift_l(XB1, XB0, i * K) >> 16;
+                const uint32_t *tw = row + j * NWD;
+                const uint32_t a0 = tw[oA0], a1 = tw[oA1];
+                const uint32_t b0 = tw[oB0], b1 = tw[oB1];
+                const uint32_t XA0 = __funnelshift_l(a1, a0, o), XB0 = __funnelshift_l(b1, b0, o);
+                uint32_t XA1 = 0, XB1 = 0;
+                if (W3) {
+                    const uint32_t a2 = tw[oA2], b2 = tw[oB2];
+                    XA1 = __funnelshift_l(a2, a1, o);
+                    XB1 = __funnelshift_l(b2, b1, o);
                 }
+                uint32_t sA[4], sB[4];
+                sA[0] = run_state<K, 0>(XA0, XA1);
+                sA[1] = run_state<K, 1>(XA0, XA1);
+                sA[2] = run_state<K, 2>(XA0, XA1);
+                sA[3] = run_state<K, 3>(XA0, XA1);
+                sB[0] = run_state<K, 0>(XB0, XB1);
+                sB[1] = run_state<K, 1>(XB0, XB1);
+                sB[2] = run_state<K, 2>(XB0, XB1);
+                sB[3] = run_state<K, 3>(XB0, XB1);
                 if (MUL1) {
                     uint32_t dA[4], dB[4];
 #pragma unroll
@@ -365,8 +405,8 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
                     uint32_t xA[4], xB[4];
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        xA[i] = lop_mask_xor(sA[i] * mul + add);
-                        xB[i] = lop_mask_xor(sB[i] * mul + add);
+                        xA[i] = ((sA[i] * mul + add) & 0x8FFF8FFFu) ^ 0x3B603B60u;
+                        xB[i] = ((sB[i] * mul + add) & 0x8FFF8FFFu) ^ 0x3B603B60u;
                     }
 #pragma unroll
                     for (int nb = 0; nb < NRB; nb++) {
@@ -385,13 +425,14 @@ __device__ __forceinline__ void dispatch_pass(float (&acc)[NRB][8][4], Ring &rin
                                               const GemmArgs &a, int warp, const Pass &ps,
                                               int chunk, const uint16_t *act_s)
 {
-    const bool mul1 = ps.cb == EXL3_CB_MUL1;
-#define EXL3_K_CASE(KK)                                                                     \
-    case KK:                                                                                \
-        if (mul1)                                                                           \
-            run_pass<KK, true, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s);  \
-        else                                                                                \
-            run_pass<KK, false, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s); \
+#define EXL3_K_CASE(KK)                                                                        \
+    case KK:                                                                                   \
+        if (ps.cb == EXL3_CB_MUL1)                                                             \
+            run_pass<KK, EXL3_CB_MUL1, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s);  \
+        else if (ps.cb == EXL3_CB_3INST)                                                       \
+            run_pass<KK, EXL3_CB_3INST, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s); \
+        else                                                                                   \
+            run_pass<KK, EXL3_CB_MCG, MODE, NRB, ADD>(acc, ring, a, warp, ps, chunk, act_s);   \
         break;
     switch (ps.K) {
         EXL3_K_CASE(1)
@@ -425,7 +466,7 @@ __device__ __forceinline__ int zs_index(int e, int frag)
 }
 
 template <int MODE, int NRB, bool ADD>
-__global__ void __launch_bounds__(kThreads, NRB == 1 ? 2 : 1) k_expert_gemm(GemmArgs a)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm(GemmArgs a)
 {
     using T = ModeTraits<MODE>;
     using S = SmemPlan<MODE, NRB>;
@@ -463,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, NRB == 1 ? 2 : 1) k_expert_gemm(Gemm
 
     Ring ring;
     ring.bar = bars + warp * kSlots;
-    ring.buf = ring_base + warp * kSlots * kSlotBytes;
+    ring.buf = ring_base + warp * kSlots * kSlotBytes;   // shared memory
     ring.ws = reinterpret_cast<WarpStream *>(smem + S::ws_off) + warp;
     ring.head = 0;
     ring.dead = false;
@@ -651,87 +692,24 @@ __global__ void __launch_bounds__(kThreads, NRB == 1 ? 2 : 1) k_expert_gemm(Gemm
         named_barrier(1, kThreads);
 
         // ---- epilogue: one warp per row, lane l owns outputs 4l..4l+3 of the block
-        const int col = it.nbk * kHb + 4 * lane;
         for (int r = warp; r < it.nrows; r += kWarps) {
             if (MODE == kModeGateUp) {
-                const int e = it.e;
-                float gv[4], uv[4], sv[4], sc[4], h[4];
+                float gv[4], uv[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     gv[i] = zs[r * kZsLd + 4 * lane + i];
                     uv[i] = zs[(ROWS + r) * kZsLd + 4 * lane + i];
                 }
-                warp_hadamard128(gv);
-                warp_hadamard128(uv);
-                load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 0]), col, sv);
-                load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 0]), col, sc);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    gv[i] = gv[i] * kInvSqrt128 * sv[i] * sc[i];
-                load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 1]), col, sv);
-                load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 1]), col, sc);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    uv[i] = uv[i] * kInvSqrt128 * sv[i] * sc[i];
-                load_half4(reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + 2]), col, sv);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    h[i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i] * sv[i];
-                warp_hadamard128(h);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    h[i] *= kInvSqrt128;
-                store_act4(a.ad, (size_t)(it.row0 + r) * a.out_f + col, EXL3_F16, h);
+                epi_gateup_row(a, it.e, it.nbk, it.row0 + r, gv, uv);
             } else {
-                const uint16_t *svh, *scl;
-                if (MODE == kModeLinear) {
-                    svh = a.lin.svh;
-                    scl = a.lin.scale;
-                } else {
-                    svh = reinterpret_cast<const uint16_t *>(a.t_svh[it.e * 3 + 2]);
-                    scl = reinterpret_cast<const uint16_t *>(a.t_scale[it.e * 3 + 2]);
-                }
-                float z[4], sv[4], sc[4];
+                float z[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++)
                     z[i] = zs[r * kZsLd + 4 * lane + i];
-                warp_hadamard128(z);
-                load_half4(svh, col, sv);
-                load_half4(scl, col, sc);
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
-                if (MODE == kModeLinear) {
-                    store_act4(a.out, (size_t)(it.row0 + r) * a.out_f + col, a.act_dtype, z);
-                } else {
-                    const int f = a.packed[it.row0 + r];
-                    const int tok = f / a.topk;
-                    *reinterpret_cast<float4 *>(a.stage + (size_t)f * a.out_f + col) =
-                        make_float4(z[0], z[1], z[2], z[3]);
-                    __threadfence();
-                    __syncwarp();
-                    int old = 0;
-                    if (lane == 0)
-                        old = atomicAdd(&a.cnt_comb[tok * a.nb + it.nbk], 1);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old == a.topk - 1) {
-                        // every route of this token has its block: combine in j order
-                        __threadfence();
-                        float o4[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int j = 0; j < a.topk; j++) {
-                            const float w = load_act(a.rw, (size_t)tok * a.topk + j, a.rw_dtype);
-                            const float4 d = __ldcg(reinterpret_cast<const float4 *>(
-                                a.stage + ((size_t)tok * a.topk + j) * a.out_f + col));
-                            o4[0] = __fmaf_rn(w, d.x, o4[0]);
-                            o4[1] = __fmaf_rn(w, d.y, o4[1]);
-                            o4[2] = __fmaf_rn(w, d.z, o4[2]);
-                            o4[3] = __fmaf_rn(w, d.w, o4[3]);
-                        }
-                        store_act4(a.out, (size_t)tok * a.out_f + col, a.act_dtype, o4);
-                        if (lane == 0)
-                            a.cnt_comb[tok * a.nb + it.nbk] = 0;
-                    }
-                }
+                if (MODE == kModeLinear)
+                    epi_linear_row(a, it.nbk, it.row0 + r, z);
+                else
+                    epi_down_row(a, it.e, it.nbk, it.row0 + r, z);
             }
         }
         named_barrier(1, kThreads);
@@ -749,9 +727,14 @@ cudaError_t launch_one(const GemmArgs &a, int grid, cudaStream_t s)
 template <int MODE, int NRB, bool ADD>
 cudaError_t set_attr_one()
 {
+    cudaError_t e = cudaFuncSetAttribute(k_expert_gemm<MODE, NRB, ADD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SmemPlan<MODE, NRB>::total);
+    if (e != cudaSuccess)
+        return e;
     return cudaFuncSetAttribute(k_expert_gemm<MODE, NRB, ADD>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SmemPlan<MODE, NRB>::total);
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
 }
 
 }  // namespace gemm

@@ -1,0 +1,517 @@
+// Prefill-regime grouped GEMM on the 5th-generation tensor cores (tcgen05 +
+// TMEM), for the gate/up and down projections of the fused EXL3 MoE layer.
+//
+// Follows "EXL3 linear and grouped routed experts" (TensorFold #837), "What this
+// changes" (trellis decode, grouped experts, gate and up, SwiGLU, down, the
+// weighted combine, a width per expert).  The pages' kernels decode into
+// mma.m16n8k16 fragments; on sm_103a the decoded tile goes to shared memory
+// and one thread drives tcgen05.mma, so the integer decode and the tensor
+// work run concurrently.
+//
+// Work item = (up to 256 routes of one expert, 128-output block); the whole
+// contraction runs in one CTA (one persistent CTA per SM).  Roles:
+//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 6-slot
+//               ring (mbarrier complete_tx);
+//   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
+//               256 columns = routes each); lane 0 issues tcgen05.mma
+//               (M=128, N=routes rounded up to 16, K=16) per stage and
+//               tcgen05.commit to release the stage;
+//   warps 2-17  decode: each thread turns one 16-state trellis column run
+//               (16 consecutive inputs of one output) into 16 fp16 weights
+//               (the two halves of the mcg/3inst word summed in fp16, mul1 as
+//               the exact integer byte sum - 510) and stores them, 16 bytes at
+//               a time, into a K-major no-swizzle A tile; they also copy the
+//               stage's activation rows (cp.async) into the K-major B tile,
+//               and after the last stage read TMEM (tcgen05.ld), transpose
+//               16 routes at a time through shared memory and run the per-row
+//               epilogues shared with the decode-regime kernel.
+// Operand layout (K-major, no swizzle): element (r, k) of a stage tile sits at
+// (r/8)*SBO + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes, SBO = (KS/8)*128.
+#pragma once
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace exl3 {
+namespace tc {
+
+constexpr int kNT = 256;          // routes per work item (MMA N upper bound)
+constexpr int kStages = 3;        // A/B operand stages
+constexpr int kTwSlots = 6;       // trellis word slots
+constexpr int kTwSlotBytes = 8192;
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kThreads = kDecThreads + 64;
+constexpr int kEpiRows = 16;
+constexpr int kZsLd = kHb + 4;
+
+template <int MODE>
+struct Traits {
+    static constexpr int nproj = (MODE == kModeGateUp) ? 2 : 1;
+    static constexpr int KS = (MODE == kModeGateUp) ? 32 : 64;   // inputs per stage
+    static constexpr int T = KS / 16;                            // trellis rows per stage
+    static constexpr int SBO = (KS / 8) * 128;
+    static constexpr int a_bytes = 128 * KS * 2;                 // per projection
+    static constexpr int b_bytes = kNT * KS * 2;
+    // shared memory map
+    static constexpr int off_a = 0;
+    static constexpr int off_b = off_a + kStages * nproj * a_bytes;
+    static constexpr int off_tw = off_b + kStages * nproj * b_bytes;
+    static constexpr int off_zs = off_tw + kTwSlots * kTwSlotBytes;
+    static constexpr int off_bar = off_zs + nproj * kEpiRows * kZsLd * 4;
+    static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2;
+    static constexpr int off_misc = off_bar + nbar * 8;
+    static constexpr int total = off_misc + 64;
+};
+
+struct Bars {
+    uint64_t *full, *empty, *twfull, *twempty, *accfull, *accempty;
+};
+
+// Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
+// as soon as another thread has given up, and then reports false.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         int32_t *hdr)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort)
+            return false;
+        if (clock64() - t0 > (1ll << 31)) {
+            *abort = 1;
+            set_error(hdr, EXL3_DERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((128u >> 4) & 0x3FFF) << 16;        // K-adjacent core matrices
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;         // 8-row groups
+    d |= (uint64_t)1 << 46;                              // tcgen05 descriptor version
+    return d;                                            // no swizzle
+}
+
+__device__ __forceinline__ uint32_t instr_desc(int n)
+{
+    // f32 accumulate, f16 A and B, both K-major, M = 128, N = n
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int NREG>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NREG])
+{
+    if (NREG == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                       "=r"(v[6]), "=r"(v[7])
+                     : "r"(taddr));
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                     : "r"(taddr));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b)
+{
+    __half2 x = *reinterpret_cast<__half2 *>(&a), y = *reinterpret_cast<__half2 *>(&b);
+    x = __hadd2(x, y);
+    return *reinterpret_cast<uint32_t *>(&x);
+}
+
+__device__ __forceinline__ uint32_t hsub1534(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    h = __hsub2(h, __half2(__ushort_as_half(0x65FE), __ushort_as_half(0x65FE)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 16 consecutive trellis states of tile column c (inputs 0..15 of one output)
+// -> 16 fp16 weights in k order, packed as 8 half2 words.
+template <int K, int CB>
+__device__ __forceinline__ void decode_column(const uint32_t *tile, int c, uint32_t w[8])
+{
+    constexpr int NWD = 8 * K;
+    constexpr int LEN = 16 + 15 * K;          // window bits of the 16 states
+    constexpr int NX = (LEN + 31) / 32;       // normalised 32-bit words
+    constexpr uint32_t A = CB == EXL3_CB_MUL1 ? 0x83DCD12Du : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
+    constexpr uint32_t B = CB == EXL3_CB_3INST ? 64248484u : 0u;
+    const int start = (16 * c + 1) * K - 16;  // cyclic: negative for c == 0
+    const int w0 = start >> 5, o = start & 31;
+    uint32_t W[NX + 1];
+#pragma unroll
+    for (int j = 0; j <= NX; j++) {
+        int idx = w0 + j;
+        idx = idx < 0 ? idx + NWD : (idx >= NWD ? idx - NWD : idx);
+        W[j] = tile[idx];
+    }
+    uint32_t X[NX + 1];
+#pragma unroll
+    for (int j = 0; j < NX; j++)
+        X[j] = __funnelshift_l(W[j + 1], W[j], o);
+    X[NX] = 0;
+    uint32_t x[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const int bit = i * K, q = bit >> 5, r = bit & 31;
+        const uint32_t s = (r + 16 <= 32) ? ((X[q] >> (16 - r)) & 0xFFFFu)
+                                          : (__funnelshift_l(X[q + 1], X[q], r) >> 16);
+        if (CB == EXL3_CB_MUL1)
+            x[i] = __dp4a(s * A, 0x01010101u, 0x6400u);
+        else
+            x[i] = ((s * A + B) & 0x8FFF8FFFu) ^ 0x3B603B60u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        if (CB == EXL3_CB_MUL1)
+            w[i] = hsub1534(prmt(x[2 * i], x[2 * i + 1], 0x5410));
+        else
+            w[i] = hadd2_u32(prmt(x[2 * i], x[2 * i + 1], 0x5410), prmt(x[2 * i], x[2 * i + 1], 0x7632));
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void decode_dispatch_cb(int cb, const uint32_t *tile, int c, uint32_t w[8])
+{
+    if (cb == EXL3_CB_MUL1)
+        decode_column<K, EXL3_CB_MUL1>(tile, c, w);
+    else if (cb == EXL3_CB_3INST)
+        decode_column<K, EXL3_CB_3INST>(tile, c, w);
+    else
+        decode_column<K, EXL3_CB_MCG>(tile, c, w);
+}
+
+__device__ __forceinline__ void decode_dispatch(int K, int cb, const uint32_t *tile, int c, uint32_t w[8])
+{
+    switch (K) {
+        case 1: decode_dispatch_cb<1>(cb, tile, c, w); break;
+        case 2: decode_dispatch_cb<2>(cb, tile, c, w); break;
+        case 3: decode_dispatch_cb<3>(cb, tile, c, w); break;
+        case 4: decode_dispatch_cb<4>(cb, tile, c, w); break;
+        case 5: decode_dispatch_cb<5>(cb, tile, c, w); break;
+        case 6: decode_dispatch_cb<6>(cb, tile, c, w); break;
+        case 7: decode_dispatch_cb<7>(cb, tile, c, w); break;
+        default: decode_dispatch_cb<8>(cb, tile, c, w); break;
+    }
+}
+
+struct TcItem {
+    int e, row0, nrows, nbk;
+};
+
+template <int MODE>
+__device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
+{
+    TcItem it;
+    const int rgi = item / a.nb;
+    it.nbk = item % a.nb;
+    const int4 r = static_cast<const int4 *>(a.rg)[rgi];
+    it.e = r.x;
+    it.row0 = r.y;
+    it.nrows = r.z;
+    return it;
+}
+
+template <int MODE>
+__device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? p : 2; }
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
+{
+    using T = Traits<MODE>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Bars B;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::off_bar);
+    B.full = bars;
+    B.empty = bars + kStages;
+    B.twfull = bars + 2 * kStages;
+    B.twempty = bars + 2 * kStages + kTwSlots;
+    B.accfull = bars + 2 * kStages + 2 * kTwSlots;
+    B.accempty = B.accfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::off_misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
+
+    const int n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
+    if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
+        const size_t n = (size_t)a.M_tokens * a.out_f;
+        for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n; i += (size_t)gridDim.x * kThreads)
+            reinterpret_cast<uint16_t *>(a.out)[i] = 0;
+        return;
+    }
+    if ((int)blockIdx.x >= n_items)
+        return;
+    const int nst = a.in_f / T::KS;                 // stages per item
+    const int ntn = a.out_f / 16;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&B.full[s], kDecThreads);
+            mbar_init(&B.empty[s], 1);
+        }
+        for (int s = 0; s < kTwSlots; s++) {
+            mbar_init(&B.twfull[s], 1);
+            mbar_init(&B.twempty[s], kDecThreads);
+        }
+        mbar_init(B.accfull, 1);
+        mbar_init(B.accempty, kDecThreads);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(tmem_slot)), "r"(T::nproj * kNT) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer: trellis rows -> word slots
+        if (lane == 0) {
+            uint32_t g = 0;
+            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
+                const TcItem it = tc_item<MODE>(a, item);
+                const uint32_t *tr[2];
+                int Kp[2];
+                uint32_t bytes = 0;
+                for (int p = 0; p < T::nproj; p++) {
+                    const int i = it.e * 3 + proj_index<MODE>(p);
+                    tr[p] = reinterpret_cast<const uint32_t *>(a.t_trellis[i]);
+                    Kp[p] = a.t_K[i];
+                    bytes += T::T * 256 * Kp[p];
+                }
+                for (int s = 0; s < nst; s++, g++) {
+                    const int slot = g % kTwSlots;
+                    if (g >= kTwSlots &&
+                        !wait_bar(&B.twempty[slot], ((g / kTwSlots) - 1) & 1, abort, a.hdr))
+                        break;
+                    uint8_t *dst = smem + T::off_tw + slot * kTwSlotBytes;
+                    mbar_arrive_expect_tx(&B.twfull[slot], bytes);
+                    for (int p = 0; p < T::nproj; p++)
+                        for (int t = 0; t < T::T; t++) {
+                            const int tk = s * T::T + t;
+                            const uint32_t *src = tr[p] + ((size_t)tk * ntn + (size_t)it.nbk * 8) * (8 * Kp[p]);
+                            bulk_g2s(dst + (p * T::T + t) * 2048, src, 256 * Kp[p], &B.twfull[slot]);
+                        }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0, nit = 0;
+            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
+                const TcItem it = tc_item<MODE>(a, item);
+                const int n_mma = max(16, (it.nrows + 15) & ~15);
+                const uint32_t idesc = instr_desc(n_mma);
+                if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
+                    break;
+                fence_after();
+                for (int s = 0; s < nst; s++, g++) {
+                    const int slot = g % kStages;
+                    if (!wait_bar(&B.full[slot], (g / kStages) & 1, abort, a.hdr))
+                        break;
+                    fence_after();
+                    for (int p = 0; p < T::nproj; p++) {
+                        const uint32_t abase = smem_addr(smem + T::off_a + (slot * T::nproj + p) * T::a_bytes);
+                        const uint32_t bbase = smem_addr(smem + T::off_b + (slot * T::nproj + p) * T::b_bytes);
+#pragma unroll
+                        for (int ks = 0; ks < T::KS / 16; ks++)
+                            mma_f16(tmem + p * kNT, smem_desc(abase + ks * 256, T::SBO),
+                                    smem_desc(bbase + ks * 256, T::SBO), idesc,
+                                    (s > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&B.empty[slot]);
+                }
+                mma_commit(B.accfull);
+            }
+        }
+    } else {
+        // ---------------- decode + operand copies + epilogue (warps 2..17)
+        const int dt = tid - 64;                 // 0..511
+        const int dw = dt >> 5;                  // decode warp 0..15
+        const int p = (MODE == kModeGateUp) ? (dt >> 8) : 0;
+        const int t = (MODE == kModeGateUp) ? ((dt >> 7) & 1) : (dt >> 7);
+        const int m = dt & 127;
+        float *zs = reinterpret_cast<float *>(smem + T::off_zs);
+        uint32_t g = 0, nit = 0;
+        for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
+            const TcItem it = tc_item<MODE>(a, item);
+            const int pi = it.e * 3 + proj_index<MODE>(p);
+            const int K = a.t_K[pi], cb = a.t_cb[pi];
+            // activation rows of stage s -> B tile of its slot (16-byte cp.async)
+            auto load_b = [&](int s, int slot) {
+                constexpr int CPR = T::KS / 8;                  // 16-byte chunks per row
+                const int nchunk = T::nproj * it.nrows * CPR;
+                for (int ch = dt; ch < nchunk; ch += kDecThreads) {
+                    const int kc = ch % CPR, rest = ch / CPR;
+                    const int n = rest % it.nrows, pp = rest / it.nrows;
+                    const uint16_t *src = a.act + (size_t)(it.row0 + n) * a.act_row_stride +
+                                          (size_t)pp * a.in_f + s * T::KS + kc * 8;
+                    const uint32_t dst = smem_addr(smem + T::off_b + (slot * T::nproj + pp) * T::b_bytes +
+                                                   (n >> 3) * T::SBO + kc * 128 + (n & 7) * 16);
+                    cp_async16(dst, src);
+                }
+                cp_async_commit();
+            };
+            {
+                const int slot = g % kStages;
+                if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
+                    break;
+                load_b(0, slot);
+            }
+            for (int s = 0; s < nst; s++, g++) {
+                const int slot = g % kStages;
+                const int tws = g % kTwSlots;
+                if (!wait_bar(&B.twfull[tws], (g / kTwSlots) & 1, abort, a.hdr))
+                    break;
+                // decode this thread's column run of tile (s*T + t, nbk*8 + m/16)
+                const uint32_t *tile = reinterpret_cast<const uint32_t *>(
+                                           smem + T::off_tw + tws * kTwSlotBytes + (p * T::T + t) * 2048) +
+                                       (m >> 4) * 8 * K;
+                uint32_t w[8];
+                decode_dispatch(K, cb, tile, m & 15, w);
+                mbar_arrive(&B.twempty[tws]);
+                uint8_t *abuf = smem + T::off_a + (slot * T::nproj + p) * T::a_bytes +
+                                (m >> 3) * T::SBO + (m & 7) * 16;
+                *reinterpret_cast<uint4 *>(abuf + (2 * t) * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(abuf + (2 * t + 1) * 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                // next stage's activations, once its slot is free
+                if (s + 1 < nst) {
+                    const int nslot = (g + 1) % kStages;
+                    if (g + 1 >= kStages &&
+                        !wait_bar(&B.empty[nslot], (((g + 1) / kStages) - 1) & 1, abort, a.hdr))
+                        break;
+                    load_b(s + 1, nslot);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&B.full[slot]);
+            }
+            if (*abort)
+                break;
+            // ---- epilogue: TMEM -> shared (16 routes at a time) -> per-row epilogue
+            if (!wait_bar(B.accfull, nit & 1, abort, a.hdr))
+                break;
+            fence_after();
+            const int q = (warp & 3);                 // TMEM lane quarter of this warp
+            float fac[2];
+            for (int pp = 0; pp < T::nproj; pp++)
+                fac[pp] = (a.t_cb[it.e * 3 + proj_index<MODE>(pp)] == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+            for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
+                if (MODE == kModeGateUp) {
+                    const int pp = dw >> 3, half = (dw & 7) >> 2;
+                    uint32_t v[8];
+                    tmem_ld<8>(tmem + ((uint32_t)(32 * q) << 16) + pp * kNT + r0 + half * 8, v);
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        zs[(pp * kEpiRows + half * 8 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[pp];
+                } else {
+                    const int cq = dw >> 2;
+                    uint32_t v[4];
+                    tmem_ld<4>(tmem + ((uint32_t)(32 * q) << 16) + r0 + cq * 4, v);
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        zs[(cq * 4 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[0];
+                }
+                named_barrier(1, kDecThreads);
+                const int r = r0 + dw;
+                if (r < it.nrows) {
+                    if (MODE == kModeGateUp) {
+                        float gv[4], uv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            gv[i] = zs[dw * kZsLd + 4 * lane + i];
+                            uv[i] = zs[(kEpiRows + dw) * kZsLd + 4 * lane + i];
+                        }
+                        epi_gateup_row(a, it.e, it.nbk, it.row0 + r, gv, uv);
+                    } else {
+                        float z[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++)
+                            z[i] = zs[dw * kZsLd + 4 * lane + i];
+                        epi_down_row(a, it.e, it.nbk, it.row0 + r, z);
+                    }
+                }
+                named_barrier(1, kDecThreads);
+            }
+            fence_before();
+            mbar_arrive(B.accempty);
+        }
+        cp_async_wait<0>();
+    }
+
+    // teardown: the MMA warp frees TMEM once the last accumulator was read
+    __syncwarp();
+    fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(T::nproj * kNT) : "memory");
+    }
+}
+
+template <int MODE>
+cudaError_t launch_tc(const GemmArgs &a, int grid, cudaStream_t s)
+{
+    k_expert_tc<MODE><<<grid, kThreads, Traits<MODE>::total, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t set_attr_tc()
+{
+    cudaError_t e = cudaFuncSetAttribute(k_expert_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Traits<MODE>::total);
+    if (e != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(k_expert_tc<MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+}  // namespace tc
+}  // namespace exl3

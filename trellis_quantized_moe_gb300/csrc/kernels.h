@@ -89,11 +89,14 @@ cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s);
 cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_tc_gateup(const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_tc_down(const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t tc_set_attributes();
+int tc_rows_per_item();
 cudaError_t gemm_gateup_set_attributes();
 cudaError_t gemm_down_set_attributes();
 cudaError_t gemm_linear_set_attributes();
-// resident CTAs per SM of the GEMM kernels for 8- and 16-row items
-constexpr int kGemmCtasPerSm8 = 2;
-constexpr int kGemmCtasPerSm16 = 1;
+// resident CTAs per SM of the GEMM kernels: 8-row items (3, additive 2), 16-row items 1
+constexpr int gemm_ctas_per_sm(int nrb, bool additive) { return nrb == 2 ? 1 : (additive ? 2 : 3); }
 
 }  // namespace exl3

@@ -1,0 +1,24 @@
+// Prefill-regime (tcgen05 / TMEM) gate/up and down kernels (see expert_tc.cuh).
+#include "expert_tc.cuh"
+
+namespace exl3 {
+
+cudaError_t launch_tc_gateup(const GemmArgs &a, int grid, cudaStream_t s)
+{
+    return tc::launch_tc<kModeGateUp>(a, grid, s);
+}
+
+cudaError_t launch_tc_down(const GemmArgs &a, int grid, cudaStream_t s)
+{
+    return tc::launch_tc<kModeDown>(a, grid, s);
+}
+
+cudaError_t tc_set_attributes()
+{
+    cudaError_t e = tc::set_attr_tc<kModeGateUp>();
+    return e != cudaSuccess ? e : tc::set_attr_tc<kModeDown>();
+}
+
+int tc_rows_per_item() { return tc::kNT; }
+
+}  // namespace exl3
