@@ -262,9 +262,9 @@ def run_ours(args):
         kern = np.array([p.times_ms() for p in profs]) if profile else None
         return ms, kern, wall
 
-    if args.case == "decode":
-        # one decode-shaped case at args.M (profiling target); short JSON
-        w = MoEWorkload(config(1, M=args.M))
+    if args.case in ("decode", "prefill"):
+        # one case at args.M (profiling target); short JSON
+        w = MoEWorkload(config(1 if args.case == "decode" else 3, M=args.M))
         ex = X.DeviceExperts.from_workload(w)
         s = w.spec
         ws = torch.empty(X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter,
@@ -274,7 +274,7 @@ def run_ours(args):
                             args.steps, args.warmup, profile=True)
         assert X.exl3_workspace_error(ws) == 0
         t = float(np.mean(ms))
-        print(json.dumps({"case": f"decode M={args.M}", "us": 1e3 * t,
+        print(json.dumps({"case": f"{args.case} M={args.M}", "us": 1e3 * t,
                           "tokens_per_s": args.M / (t * 1e-3),
                           "layer_gbs": _layer_bytes(w, w.ids) / (t * 1e-3) / 1e9,
                           "kernel_us": [1e3 * float(v) for v in kern.mean(axis=0)]}))
@@ -400,8 +400,8 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--case", default="all", choices=["all", "decode"],
-                    help="decode: only the decode-shaped layer at --M (profiling target)")
+    ap.add_argument("--case", default="all", choices=["all", "decode", "prefill"],
+                    help="decode / prefill: only that layer at --M (profiling target)")
     ap.add_argument("--M", type=int, default=1)
     args = ap.parse_args()
     if args.impl == "reference":
