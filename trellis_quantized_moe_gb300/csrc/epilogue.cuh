@@ -88,6 +88,57 @@ __device__ __forceinline__ void epi_down_row(const GemmArgs &a, int e, int nbk, 
     }
 }
 
+// The down epilogue in two phases, for kernels that stage many rows and then
+// publish them with a single fence: (1) d = Hb(z)*svh*scale into the staging
+// row; (2) after a __threadfence by every staging thread, count the route and
+// combine the token's block if it was the last one.
+__device__ __forceinline__ void epi_down_stage_row(const GemmArgs &a, int e, int nbk, int prow,
+                                                   float z[4])
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    const uint16_t *svh = reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 2]);
+    const uint16_t *scl = reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 2]);
+    float sv[4], sc[4];
+    warp_hadamard128(z);
+    load_half4(svh, col, sv);
+    load_half4(scl, col, sc);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
+    const int f = a.packed[prow];
+    *reinterpret_cast<float4 *>(a.stage + (size_t)f * a.out_f + col) =
+        make_float4(z[0], z[1], z[2], z[3]);
+}
+
+__device__ __forceinline__ void epi_down_combine_row(const GemmArgs &a, int nbk, int prow)
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    const int f = a.packed[prow];
+    const int tok = f / a.topk;
+    int old = 0;
+    if (lane == 0)
+        old = atomicAdd(&a.cnt_comb[tok * a.nb + nbk], 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == a.topk - 1) {
+        __threadfence();
+        float o4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < a.topk; j++) {
+            const float w = load_act(a.rw, (size_t)tok * a.topk + j, a.rw_dtype);
+            const float4 d = __ldcg(reinterpret_cast<const float4 *>(
+                a.stage + ((size_t)tok * a.topk + j) * a.out_f + col));
+            o4[0] = __fmaf_rn(w, d.x, o4[0]);
+            o4[1] = __fmaf_rn(w, d.y, o4[1]);
+            o4[2] = __fmaf_rn(w, d.z, o4[2]);
+            o4[3] = __fmaf_rn(w, d.w, o4[3]);
+        }
+        store_act4(a.out, (size_t)tok * a.out_f + col, a.act_dtype, o4);
+        if (lane == 0)
+            a.cnt_comb[tok * a.nb + nbk] = 0;
+    }
+}
+
 // linear: y = Hb(z)*svh*scale, stored in the activation dtype.
 __device__ __forceinline__ void epi_linear_row(const GemmArgs &a, int nbk, int row, float z[4])
 {

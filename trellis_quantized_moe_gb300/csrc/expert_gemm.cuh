@@ -310,9 +310,10 @@ __device__ __forceinline__ uint32_t hsub_1534(uint32_t v)
 template <int K, int I>
 __device__ __forceinline__ uint32_t run_state(uint32_t X0, uint32_t X1)
 {
-    if (I * K + 16 <= 32)
+    if constexpr (I * K + 16 <= 32)
         return (X0 >> (16 - I * K)) & 0xFFFFu;
-    return __funnelshift_l(X1, X0, I * K) >> 16;
+    else
+        return __funnelshift_l(X1, X0, I * K) >> 16;
 }
 
 // codebook constants: x = a*s + b (mod 2^32)

@@ -164,35 +164,53 @@ __device__ __forceinline__ uint32_t hsub1534(uint32_t v)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 16 consecutive trellis states of tile column c (inputs 0..15 of one output)
-// -> 16 fp16 weights in k order, packed as 8 half2 words.
+// Word offsets (inside a tile) and bit shift of the window holding the 16
+// consecutive trellis states of tile column c (inputs 0..15 of one output);
+// the window is cyclic, so column 0 starts in the tile's last word.
+template <int K>
+struct ColumnWindow {
+    static constexpr int NWD = 8 * K;
+    static constexpr int LEN = 16 + 15 * K;     // window bits of the 16 states
+    static constexpr int NX = (LEN + 31) / 32;  // normalised 32-bit words
+    int idx[NX + 1];
+    int o;
+    __device__ __forceinline__ explicit ColumnWindow(int c)
+    {
+        const int start = (16 * c + 1) * K - 16;
+        const int w0 = start >> 5;
+        o = start & 31;
+#pragma unroll
+        for (int j = 0; j <= NX; j++) {
+            int v = w0 + j;
+            idx[j] = v < 0 ? v + NWD : (v >= NWD ? v - NWD : v);
+        }
+    }
+};
+
+// The 16 states of the window -> 16 fp16 weights in k order (8 half2 words):
+// mcg/3inst sum their two fp16 halves in fp16 (one rounding), mul1 gives the
+// exact integer byte sum - 510.
 template <int K, int CB>
-__device__ __forceinline__ void decode_column(const uint32_t *tile, int c, uint32_t w[8])
+__device__ __forceinline__ void decode_column(const uint32_t *tile, const ColumnWindow<K> &cw,
+                                              uint32_t w[8])
 {
-    constexpr int NWD = 8 * K;
-    constexpr int LEN = 16 + 15 * K;          // window bits of the 16 states
-    constexpr int NX = (LEN + 31) / 32;       // normalised 32-bit words
+    constexpr int NX = ColumnWindow<K>::NX;
     constexpr uint32_t A = CB == EXL3_CB_MUL1 ? 0x83DCD12Du : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
     constexpr uint32_t B = CB == EXL3_CB_3INST ? 64248484u : 0u;
-    const int start = (16 * c + 1) * K - 16;  // cyclic: negative for c == 0
-    const int w0 = start >> 5, o = start & 31;
     uint32_t W[NX + 1];
 #pragma unroll
-    for (int j = 0; j <= NX; j++) {
-        int idx = w0 + j;
-        idx = idx < 0 ? idx + NWD : (idx >= NWD ? idx - NWD : idx);
-        W[j] = tile[idx];
-    }
+    for (int j = 0; j <= NX; j++)
+        W[j] = tile[cw.idx[j]];
     uint32_t X[NX + 1];
 #pragma unroll
     for (int j = 0; j < NX; j++)
-        X[j] = __funnelshift_l(W[j + 1], W[j], o);
+        X[j] = __funnelshift_l(W[j + 1], W[j], cw.o);
     X[NX] = 0;
     uint32_t x[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
         const int bit = i * K, q = bit >> 5, r = bit & 31;
-        const uint32_t s = (r + 16 <= 32) ? ((X[q] >> (16 - r)) & 0xFFFFu)
+        const uint32_t s = (r + 16 <= 32) ? ((X[q] >> ((16 - r) & 31)) & 0xFFFFu)
                                           : (__funnelshift_l(X[q + 1], X[q], r) >> 16);
         if (CB == EXL3_CB_MUL1)
             x[i] = __dp4a(s * A, 0x01010101u, 0x6400u);
@@ -208,29 +226,11 @@ __device__ __forceinline__ void decode_column(const uint32_t *tile, int c, uint3
     }
 }
 
-template <int K>
-__device__ __forceinline__ void decode_dispatch_cb(int cb, const uint32_t *tile, int c, uint32_t w[8])
+__device__ __forceinline__ void warp_arrive(uint64_t *bar)
 {
-    if (cb == EXL3_CB_MUL1)
-        decode_column<K, EXL3_CB_MUL1>(tile, c, w);
-    else if (cb == EXL3_CB_3INST)
-        decode_column<K, EXL3_CB_3INST>(tile, c, w);
-    else
-        decode_column<K, EXL3_CB_MCG>(tile, c, w);
-}
-
-__device__ __forceinline__ void decode_dispatch(int K, int cb, const uint32_t *tile, int c, uint32_t w[8])
-{
-    switch (K) {
-        case 1: decode_dispatch_cb<1>(cb, tile, c, w); break;
-        case 2: decode_dispatch_cb<2>(cb, tile, c, w); break;
-        case 3: decode_dispatch_cb<3>(cb, tile, c, w); break;
-        case 4: decode_dispatch_cb<4>(cb, tile, c, w); break;
-        case 5: decode_dispatch_cb<5>(cb, tile, c, w); break;
-        case 6: decode_dispatch_cb<6>(cb, tile, c, w); break;
-        case 7: decode_dispatch_cb<7>(cb, tile, c, w); break;
-        default: decode_dispatch_cb<8>(cb, tile, c, w); break;
-    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(bar);
 }
 
 struct TcItem {
@@ -252,6 +252,86 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 
 template <int MODE>
 __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? p : 2; }
+
+// All stages of one work item for one decode thread: activation rows of the
+// next stage -> B tile (cp.async), trellis words -> decoded A tile, one
+// arrival per warp on the stage barrier.  K and the codebook are compile-time.
+template <int MODE, int K, int CB>
+__device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
+                                          volatile int *abort, const TcItem &it, uint32_t &g,
+                                          int dt, int p, int t, int m)
+{
+    using T = Traits<MODE>;
+    constexpr int CPR = T::KS / 8;                   // 16-byte chunks per activation row
+    constexpr int RPP = kDecThreads / CPR;           // rows covered per pass
+    const int nst = a.in_f / T::KS;
+    const ColumnWindow<K> cw(m & 15);
+    const int kc = dt % CPR, n0 = dt / CPR;
+    // this thread's activation chunks: projection pp, row n0 + RPP*i, chunk kc
+    auto load_b = [&](int s, int slot) {
+#pragma unroll
+        for (int pp = 0; pp < T::nproj; pp++)
+#pragma unroll
+            for (int i = 0; i < kNT / RPP; i++) {
+                const int n = n0 + RPP * i;
+                if (n < it.nrows) {
+                    const uint16_t *src = a.act + (size_t)(it.row0 + n) * a.act_row_stride +
+                                          (size_t)pp * a.in_f + s * T::KS + kc * 8;
+                    cp_async16(smem_addr(smem + T::off_b + (slot * T::nproj + pp) * T::b_bytes +
+                                         (n >> 3) * T::SBO + kc * 128 + (n & 7) * 16),
+                               src);
+                }
+            }
+        cp_async_commit();
+    };
+    {
+        const int slot = g % kStages;
+        if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
+            return false;
+        load_b(0, slot);
+    }
+    const int tile_off = (p * T::T + t) * 2048 + (m >> 4) * 32 * K;          // bytes
+    const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
+    for (int s = 0; s < nst; s++, g++) {
+        const int slot = g % kStages;
+        const int tws = g % kTwSlots;
+        if (!wait_bar(&B.twfull[tws], (g / kTwSlots) & 1, abort, a.hdr))
+            return false;
+        uint32_t w[8];
+        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + tws * kTwSlotBytes +
+                                                                tile_off),
+                             cw, w);
+        warp_arrive(&B.twempty[tws]);
+        uint8_t *abuf = smem + T::off_a + slot * T::nproj * T::a_bytes + a_off;
+        *reinterpret_cast<uint4 *>(abuf) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(abuf + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+        if (s + 1 < nst) {
+            const int nslot = (g + 1) % kStages;
+            if (g + 1 >= kStages &&
+                !wait_bar(&B.empty[nslot], (((g + 1) / kStages) - 1) & 1, abort, a.hdr))
+                return false;
+            load_b(s + 1, nslot);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        warp_arrive(&B.full[slot]);
+    }
+    return true;
+}
+
+template <int MODE, int K>
+__device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t *smem, const Bars &B,
+                                             volatile int *abort, const TcItem &it, uint32_t &g,
+                                             int dt, int p, int t, int m)
+{
+    if (cb == EXL3_CB_MUL1)
+        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, g, dt, p, t, m);
+    if (cb == EXL3_CB_3INST)
+        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, g, dt, p, t, m);
+    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, g, dt, p, t, m);
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
@@ -284,15 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&B.full[s], kDecThreads);
+            mbar_init(&B.full[s], kDecWarps);
             mbar_init(&B.empty[s], 1);
         }
         for (int s = 0; s < kTwSlots; s++) {
             mbar_init(&B.twfull[s], 1);
-            mbar_init(&B.twempty[s], kDecThreads);
+            mbar_init(&B.twempty[s], kDecWarps);
         }
         mbar_init(B.accfull, 1);
-        mbar_init(B.accempty, kDecThreads);
+        mbar_init(B.accempty, kDecWarps);
         *abort = 0;
         fence_mbar_init();
     }
@@ -380,58 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
             const TcItem it = tc_item<MODE>(a, item);
             const int pi = it.e * 3 + proj_index<MODE>(p);
             const int K = a.t_K[pi], cb = a.t_cb[pi];
-            // activation rows of stage s -> B tile of its slot (16-byte cp.async)
-            auto load_b = [&](int s, int slot) {
-                constexpr int CPR = T::KS / 8;                  // 16-byte chunks per row
-                const int nchunk = T::nproj * it.nrows * CPR;
-                for (int ch = dt; ch < nchunk; ch += kDecThreads) {
-                    const int kc = ch % CPR, rest = ch / CPR;
-                    const int n = rest % it.nrows, pp = rest / it.nrows;
-                    const uint16_t *src = a.act + (size_t)(it.row0 + n) * a.act_row_stride +
-                                          (size_t)pp * a.in_f + s * T::KS + kc * 8;
-                    const uint32_t dst = smem_addr(smem + T::off_b + (slot * T::nproj + pp) * T::b_bytes +
-                                                   (n >> 3) * T::SBO + kc * 128 + (n & 7) * 16);
-                    cp_async16(dst, src);
-                }
-                cp_async_commit();
-            };
-            {
-                const int slot = g % kStages;
-                if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
-                    break;
-                load_b(0, slot);
+            bool ok;
+            switch (K) {
+                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
             }
-            for (int s = 0; s < nst; s++, g++) {
-                const int slot = g % kStages;
-                const int tws = g % kTwSlots;
-                if (!wait_bar(&B.twfull[tws], (g / kTwSlots) & 1, abort, a.hdr))
-                    break;
-                // decode this thread's column run of tile (s*T + t, nbk*8 + m/16)
-                const uint32_t *tile = reinterpret_cast<const uint32_t *>(
-                                           smem + T::off_tw + tws * kTwSlotBytes + (p * T::T + t) * 2048) +
-                                       (m >> 4) * 8 * K;
-                uint32_t w[8];
-                decode_dispatch(K, cb, tile, m & 15, w);
-                mbar_arrive(&B.twempty[tws]);
-                uint8_t *abuf = smem + T::off_a + (slot * T::nproj + p) * T::a_bytes +
-                                (m >> 3) * T::SBO + (m & 7) * 16;
-                *reinterpret_cast<uint4 *>(abuf + (2 * t) * 128) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(abuf + (2 * t + 1) * 128) = make_uint4(w[4], w[5], w[6], w[7]);
-                // next stage's activations, once its slot is free
-                if (s + 1 < nst) {
-                    const int nslot = (g + 1) % kStages;
-                    if (g + 1 >= kStages &&
-                        !wait_bar(&B.empty[nslot], (((g + 1) / kStages) - 1) & 1, abort, a.hdr))
-                        break;
-                    load_b(s + 1, nslot);
-                    cp_async_wait<1>();
-                } else {
-                    cp_async_wait<0>();
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&B.full[slot]);
-            }
-            if (*abort)
+            if (!ok || *abort)
                 break;
             // ---- epilogue: TMEM -> shared (16 routes at a time) -> per-row epilogue
             if (!wait_bar(B.accfull, nit & 1, abort, a.hdr))
@@ -473,13 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
 #pragma unroll
                         for (int i = 0; i < 4; i++)
                             z[i] = zs[dw * kZsLd + 4 * lane + i];
-                        epi_down_row(a, it.e, it.nbk, it.row0 + r, z);
+                        epi_down_stage_row(a, it.e, it.nbk, it.row0 + r, z);
                     }
                 }
                 named_barrier(1, kDecThreads);
             }
             fence_before();
-            mbar_arrive(B.accempty);
+            warp_arrive(B.accempty);
+            if (MODE == kModeDown) {
+                // all of this item's staged rows, then one fence, then the counters
+                __threadfence();
+                named_barrier(1, kDecThreads);
+                for (int r = dw; r < it.nrows; r += kDecWarps)
+                    epi_down_combine_row(a, it.nbk, it.row0 + r);
+            }
         }
         cp_async_wait<0>();
     }
