@@ -68,6 +68,50 @@ bool on_device(const void *p, int dev)
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the library
+// does not link the driver library itself); looked up once.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box height
+// 16 << i rows, box width 8; rows past the end read as zero.
+bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int i = 0; i < kTcMaps; i++) {
+        const cuuint32_t box[2] = {8, (cuuint32_t)(16 << i)};
+        if (fn(&m.act[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 bool act_dtype_ok(int d) { return d == EXL3_F16 || d == EXL3_BF16; }
 bool ids_dtype_ok(int d) { return d == EXL3_I32 || d == EXL3_I64; }
 bool rw_dtype_ok(int d) { return d == EXL3_F16 || d == EXL3_BF16 || d == EXL3_F32; }
@@ -205,7 +249,10 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.part = reinterpret_cast<float *>(w + L.part1);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
-    if ((use_tc ? launch_tc_gateup(g, sms, s) : launch_gemm_gateup(additive, nrb, g, sms * ctas, s)) !=
+    TcMaps maps1, maps2;
+    if (use_tc && (!encode_act_maps(maps1, g.act, 2 * hidden, R) || !encode_act_maps(maps2, g.ad, inter, R)))
+        return EXL3_E_CUDA;
+    if ((use_tc ? launch_tc_gateup(g, maps1, sms, s) : launch_gemm_gateup(additive, nrb, g, sms * ctas, s)) !=
         cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(3, s);
@@ -225,7 +272,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.rw_dtype = rw_dtype;
     g.cnt_comb = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = out;
-    if ((use_tc ? launch_tc_down(g, sms, s) : launch_gemm_down(additive, nrb, g, sms * ctas, s)) !=
+    if ((use_tc ? launch_tc_down(g, maps2, sms, s) : launch_gemm_down(additive, nrb, g, sms * ctas, s)) !=
         cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(4, s);

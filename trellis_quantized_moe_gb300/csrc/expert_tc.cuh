@@ -10,24 +10,29 @@
 //
 // Work item = (up to 256 routes of one expert, 128-output block); the whole
 // contraction runs in one CTA (one persistent CTA per SM).  Roles:
-//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 6-slot
-//               ring (mbarrier complete_tx);
+//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 4-slot
+//               ring (mbarrier complete_tx) and prefetches later rows to L2;
 //   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
 //               256 columns = routes each); lane 0 issues tcgen05.mma
 //               (M=128, N=routes rounded up to 16, K=16) per stage and
-//               tcgen05.commit to release the stage;
+//               tcgen05.commit to release the stage's operands;
 //   warps 2-17  decode: each thread turns one 16-state trellis column run
 //               (16 consecutive inputs of one output) into 16 fp16 weights
 //               (the two halves of the mcg/3inst word summed in fp16, mul1 as
 //               the exact integer byte sum - 510) and stores them, 16 bytes at
-//               a time, into a K-major no-swizzle A tile; they also copy the
-//               stage's activation rows (cp.async) into the K-major B tile,
-//               and after the last stage read TMEM (tcgen05.ld), transpose
-//               16 routes at a time through shared memory and run the per-row
-//               epilogues shared with the decode-regime kernel.
-// Operand layout (K-major, no swizzle): element (r, k) of a stage tile sits at
+//               a time, into a K-major no-swizzle A tile; after the last stage
+//               they read TMEM (tcgen05.ld), transpose 16 routes at a time
+//               through shared memory and run the per-row epilogues shared
+//               with the decode-regime kernel;
+//   warp 18     lane 0 loads the activation (B) tiles with 2D TMA into a byte
+//               ring that runs as far ahead of the MMAs as it has room.
+// A layout (K-major, no swizzle): element (r, k) of a stage tile sits at
 // (r/8)*SBO + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes, SBO = (KS/8)*128.
+// B layout (K-major, no swizzle, as one TMA box {8 inputs, RB rows} per 8
+// inputs): (k/8)*RB*16 + r*16 + (k%8)*2, i.e. core matrices 128 bytes apart
+// along the routes and RB*16 bytes apart along k.
 #pragma once
+#include <string.h>
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -36,12 +41,16 @@ namespace exl3 {
 namespace tc {
 
 constexpr int kNT = 256;          // routes per work item (MMA N upper bound)
-constexpr int kStages = 3;        // A/B operand stages
-constexpr int kTwSlots = 6;       // trellis word slots
+constexpr int kStages = 3;        // decoded-weight (A) stages
+constexpr int kTwSlots = 4;       // trellis word slots
+constexpr int kBRingBytes = 128 * 1024;   // activation (B) stages, sized per item
+constexpr int kMaxBSlots = 16;
+constexpr int kTwAhead = 16;      // trellis stages prefetched into L2 ahead
 constexpr int kTwSlotBytes = 8192;
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kThreads = kDecThreads + 64;
+constexpr int kBWarp = 2 + kDecWarps;     // activation producer
+constexpr int kThreads = kDecThreads + 96;
 constexpr int kEpiRows = 16;
 constexpr int kZsLd = kHb + 4;
 
@@ -52,21 +61,47 @@ struct Traits {
     static constexpr int T = KS / 16;                            // trellis rows per stage
     static constexpr int SBO = (KS / 8) * 128;
     static constexpr int a_bytes = 128 * KS * 2;                 // per projection
-    static constexpr int b_bytes = kNT * KS * 2;
     // shared memory map
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + kStages * nproj * a_bytes;
-    static constexpr int off_tw = off_b + kStages * nproj * b_bytes;
+    static constexpr int off_tw = off_b + kBRingBytes;
     static constexpr int off_zs = off_tw + kTwSlots * kTwSlotBytes;
     static constexpr int off_bar = off_zs + nproj * kEpiRows * kZsLd * 4;
-    static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2;
+    static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 2;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int total = off_misc + 64;
 };
 
 struct Bars {
-    uint64_t *full, *empty, *twfull, *twempty, *accfull, *accempty;
+    uint64_t *full, *empty, *twfull, *twempty, *bfull, *bempty, *accfull, *accempty;
 };
+
+// The activation tensor maps: one per TMA box height RB = 16, 32, ..., 256.
+struct TcMapsDev {
+    CUtensorMap act[kTcMaps];
+};
+
+// Activation ring geometry of one work item: RB = the item's routes rounded
+// up to a power of two (>= 16), one stage = nproj x KS/8 boxes of RB rows; as
+// many stages as fit in the ring (at most 16).  Items of the same geometry
+// continue one ring; a change of geometry first drains it.
+struct BGeom {
+    int rb, map, proj_bytes, stage_bytes, nslots;
+};
+
+template <int KS, int NPROJ>
+__device__ __forceinline__ BGeom b_geom(int nrows)
+{
+    BGeom g;
+    g.map = 0;
+    while ((16 << g.map) < nrows)
+        g.map++;
+    g.rb = 16 << g.map;
+    g.proj_bytes = g.rb * KS * 2;
+    g.stage_bytes = NPROJ * g.proj_bytes;
+    g.nslots = min(kMaxBSlots, kBRingBytes / g.stage_bytes);
+    return g;
+}
 
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
 // as soon as another thread has given up, and then reports false.
@@ -93,14 +128,27 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo)
+// no-swizzle K-major operand: lbo = bytes between core matrices adjacent in
+// k, sbo = bytes between 8-row groups
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
 {
     uint64_t d = 0;
     d |= (uint64_t)((addr >> 4) & 0x3FFF);
-    d |= (uint64_t)((128u >> 4) & 0x3FFF) << 16;        // K-adjacent core matrices
-    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;         // 8-row groups
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;                              // tcgen05 descriptor version
     return d;                                            // no swizzle
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_addr(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t instr_desc(int n)
@@ -126,13 +174,10 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int NREG>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NREG])
@@ -253,48 +298,25 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 template <int MODE>
 __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? p : 2; }
 
-// All stages of one work item for one decode thread: activation rows of the
-// next stage -> B tile (cp.async), trellis words -> decoded A tile, one
-// arrival per warp on the stage barrier.  K and the codebook are compile-time.
+// All stages of one work item for one decode thread: trellis words -> decoded
+// A tile, one arrival per warp on the stage barrier.  K and the codebook are
+// compile-time.
 template <int MODE, int K, int CB>
 __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
                                           volatile int *abort, const TcItem &it, uint32_t &g,
-                                          int dt, int p, int t, int m)
+                                          int p, int t, int m)
 {
     using T = Traits<MODE>;
-    constexpr int CPR = T::KS / 8;                   // 16-byte chunks per activation row
-    constexpr int RPP = kDecThreads / CPR;           // rows covered per pass
     const int nst = a.in_f / T::KS;
     const ColumnWindow<K> cw(m & 15);
-    const int kc = dt % CPR, n0 = dt / CPR;
-    // this thread's activation chunks: projection pp, row n0 + RPP*i, chunk kc
-    auto load_b = [&](int s, int slot) {
-#pragma unroll
-        for (int pp = 0; pp < T::nproj; pp++)
-#pragma unroll
-            for (int i = 0; i < kNT / RPP; i++) {
-                const int n = n0 + RPP * i;
-                if (n < it.nrows) {
-                    const uint16_t *src = a.act + (size_t)(it.row0 + n) * a.act_row_stride +
-                                          (size_t)pp * a.in_f + s * T::KS + kc * 8;
-                    cp_async16(smem_addr(smem + T::off_b + (slot * T::nproj + pp) * T::b_bytes +
-                                         (n >> 3) * T::SBO + kc * 128 + (n & 7) * 16),
-                               src);
-                }
-            }
-        cp_async_commit();
-    };
-    {
-        const int slot = g % kStages;
-        if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
-            return false;
-        load_b(0, slot);
-    }
     const int tile_off = (p * T::T + t) * 2048 + (m >> 4) * 32 * K;          // bytes
     const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
     for (int s = 0; s < nst; s++, g++) {
         const int slot = g % kStages;
         const int tws = g % kTwSlots;
+        // the A slot is free once the MMA of stage g - 3 completed
+        if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
+            return false;
         if (!wait_bar(&B.twfull[tws], (g / kTwSlots) & 1, abort, a.hdr))
             return false;
         uint32_t w[8];
@@ -305,16 +327,6 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
         uint8_t *abuf = smem + T::off_a + slot * T::nproj * T::a_bytes + a_off;
         *reinterpret_cast<uint4 *>(abuf) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4 *>(abuf + 128) = make_uint4(w[4], w[5], w[6], w[7]);
-        if (s + 1 < nst) {
-            const int nslot = (g + 1) % kStages;
-            if (g + 1 >= kStages &&
-                !wait_bar(&B.empty[nslot], (((g + 1) / kStages) - 1) & 1, abort, a.hdr))
-                return false;
-            load_b(s + 1, nslot);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         warp_arrive(&B.full[slot]);
     }
@@ -324,17 +336,17 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
 template <int MODE, int K>
 __device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t *smem, const Bars &B,
                                              volatile int *abort, const TcItem &it, uint32_t &g,
-                                             int dt, int p, int t, int m)
+                                             int p, int t, int m)
 {
     if (cb == EXL3_CB_MUL1)
-        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, g, dt, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, g, p, t, m);
     if (cb == EXL3_CB_3INST)
-        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, g, dt, p, t, m);
-    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, g, dt, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, g, p, t, m);
+    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, g, p, t, m);
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
+__global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __grid_constant__ TcMapsDev maps)
 {
     using T = Traits<MODE>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -345,7 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
     B.empty = bars + kStages;
     B.twfull = bars + 2 * kStages;
     B.twempty = bars + 2 * kStages + kTwSlots;
-    B.accfull = bars + 2 * kStages + 2 * kTwSlots;
+    B.bfull = bars + 2 * kStages + 2 * kTwSlots;
+    B.bempty = B.bfull + kMaxBSlots;
+    B.accfull = B.bempty + kMaxBSlots;
     B.accempty = B.accfull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::off_misc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
@@ -370,6 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
         for (int s = 0; s < kTwSlots; s++) {
             mbar_init(&B.twfull[s], 1);
             mbar_init(&B.twempty[s], kDecWarps);
+        }
+        for (int s = 0; s < kMaxBSlots; s++) {
+            mbar_init(&B.bfull[s], 1);
+            mbar_init(&B.bempty[s], 1);
         }
         mbar_init(B.accfull, 1);
         mbar_init(B.accempty, kDecWarps);
@@ -401,7 +419,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
                     Kp[p] = a.t_K[i];
                     bytes += T::T * 256 * Kp[p];
                 }
+                auto prefetch_stage = [&](int s) {
+                    for (int p = 0; p < T::nproj; p++)
+                        for (int t = 0; t < T::T; t++) {
+                            const int tk = s * T::T + t;
+                            prefetch_l2_bulk(tr[p] + ((size_t)tk * ntn + (size_t)it.nbk * 8) * (8 * Kp[p]),
+                                             256 * Kp[p]);
+                        }
+                };
+                for (int s = 0; s < kTwAhead && s < nst; s++)
+                    prefetch_stage(s);
                 for (int s = 0; s < nst; s++, g++) {
+                    if (s + kTwAhead < nst)
+                        prefetch_stage(s + kTwAhead);
                     const int slot = g % kTwSlots;
                     if (g >= kTwSlots &&
                         !wait_bar(&B.twempty[slot], ((g / kTwSlots) - 1) & 1, abort, a.hdr))
@@ -420,35 +450,88 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            uint32_t g = 0, nit = 0;
+            uint32_t g = 0, nit = 0, bphase = 0;     // bphase: parity bit per B slot
+            int gb = 0, cur_rb = 0;                   // B ring position, geometry
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
+                const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
+                if (bg.rb != cur_rb) {
+                    gb = 0;
+                    cur_rb = bg.rb;
+                }
                 const int n_mma = max(16, (it.nrows + 15) & ~15);
                 const uint32_t idesc = instr_desc(n_mma);
                 if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
                     break;
                 fence_after();
-                for (int s = 0; s < nst; s++, g++) {
+                for (int s = 0; s < nst; s++, g++, gb++) {
                     const int slot = g % kStages;
-                    if (!wait_bar(&B.full[slot], (g / kStages) & 1, abort, a.hdr))
+                    const int bs = gb % bg.nslots;
+                    if (!wait_bar(&B.full[slot], (g / kStages) & 1, abort, a.hdr) ||
+                        !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
                         break;
+                    bphase ^= 1u << bs;
                     fence_after();
                     for (int p = 0; p < T::nproj; p++) {
                         const uint32_t abase = smem_addr(smem + T::off_a + (slot * T::nproj + p) * T::a_bytes);
-                        const uint32_t bbase = smem_addr(smem + T::off_b + (slot * T::nproj + p) * T::b_bytes);
+                        const uint32_t bbase = smem_addr(smem + T::off_b + bs * bg.stage_bytes + p * bg.proj_bytes);
 #pragma unroll
                         for (int ks = 0; ks < T::KS / 16; ks++)
-                            mma_f16(tmem + p * kNT, smem_desc(abase + ks * 256, T::SBO),
-                                    smem_desc(bbase + ks * 256, T::SBO), idesc,
+                            mma_f16(tmem + p * kNT, smem_desc(abase + ks * 256, 128, T::SBO),
+                                    smem_desc(bbase + ks * 32 * bg.rb, 16 * bg.rb, 128), idesc,
                                     (s > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&B.empty[slot]);
+                    mma_commit(&B.bempty[bs]);
                 }
                 mma_commit(B.accfull);
             }
         }
+    } else if (warp == kBWarp) {
+        // ---------------- activation producer: 2D TMA boxes into the B ring
+        if (lane == 0) {
+            uint32_t pend = 0, ph = 0;                // per B slot: use in flight, parity
+            int gb = 0, cur_rb = 0;
+            auto reclaim = [&](int bs) -> bool {
+                if ((pend >> bs) & 1) {
+                    if (!wait_bar(&B.bempty[bs], (ph >> bs) & 1, abort, a.hdr))
+                        return false;
+                    ph ^= 1u << bs;
+                    pend &= ~(1u << bs);
+                }
+                return true;
+            };
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items && !*abort; item += gridDim.x) {
+                const TcItem it = tc_item<MODE>(a, item);
+                const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
+                if (bg.rb != cur_rb) {
+                    // slots of the old geometry overlap the new ones: drain the ring
+                    for (int bs = 0; ok && bs < kMaxBSlots; bs++)
+                        ok = reclaim(bs);
+                    gb = 0;
+                    cur_rb = bg.rb;
+                }
+                const CUtensorMap *map = &maps.act[bg.map];
+                for (int s = 0; ok && s < nst; s++, gb++) {
+                    const int bs = gb % bg.nslots;
+                    if (!(ok = reclaim(bs)))
+                        break;
+                    pend |= 1u << bs;
+                    uint8_t *dst = smem + T::off_b + bs * bg.stage_bytes;
+                    mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
+                    for (int p = 0; p < T::nproj; p++)
+#pragma unroll
+                        for (int kc = 0; kc < T::KS / 8; kc++)
+                            tma_load_2d(dst + p * bg.proj_bytes + kc * 16 * bg.rb, map,
+                                        p * a.in_f + s * T::KS + kc * 8, it.row0, &B.bfull[bs]);
+                }
+            }
+            // every load this thread issued is consumed by an MMA before the
+            // CTA ends; nothing to wait for here
+        }
     } else {
-        // ---------------- decode + operand copies + epilogue (warps 2..17)
+        // ---------------- decode + epilogue (warps 2..17)
         const int dt = tid - 64;                 // 0..511
         const int dw = dt >> 5;                  // decode warp 0..15
         const int p = (MODE == kModeGateUp) ? (dt >> 8) : 0;
@@ -462,14 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
             const int K = a.t_K[pi], cb = a.t_cb[pi];
             bool ok;
             switch (K) {
-                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
-                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, g, dt, p, t, m); break;
+                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, g, p, t, m); break;
             }
             if (!ok || *abort)
                 break;
@@ -528,9 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
                     epi_down_combine_row(a, it.nbk, it.row0 + r);
             }
         }
-        cp_async_wait<0>();
     }
 
+    // after a timeout, give copies and MMAs still in flight time to land
+    // before the shared memory and TMEM are released
+    if (*abort) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < (1ll << 21)) {
+        }
+    }
     // teardown: the MMA warp frees TMEM once the last accumulator was read
     __syncwarp();
     fence_before();
@@ -543,9 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a)
 }
 
 template <int MODE>
-cudaError_t launch_tc(const GemmArgs &a, int grid, cudaStream_t s)
+cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s)
 {
-    k_expert_tc<MODE><<<grid, kThreads, Traits<MODE>::total, s>>>(a);
+    TcMapsDev m;
+    static_assert(sizeof(m.act) == sizeof(maps.act), "tensor map table");
+    memcpy(m.act, maps.act, sizeof(m.act));
+    k_expert_tc<MODE><<<grid, kThreads, Traits<MODE>::total, s>>>(a, m);
     return cudaGetLastError();
 }
 

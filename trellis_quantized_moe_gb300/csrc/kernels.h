@@ -1,6 +1,7 @@
 // Kernel argument structs and launchers (host <-> device interface of the
 // library; internal, not part of the C ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
@@ -89,8 +90,14 @@ cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s);
 cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
-cudaError_t launch_tc_gateup(const GemmArgs &a, int grid, cudaStream_t s);
-cudaError_t launch_tc_down(const GemmArgs &a, int grid, cudaStream_t s);
+// Prefill-regime activation tensor maps: a 2D fp16 [rows][cols] view of the
+// rotated activations, one map per TMA box height 16 << i rows (box width 8).
+constexpr int kTcMaps = 5;
+struct TcMaps {
+    CUtensorMap act[kTcMaps];
+};
+cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
+cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t tc_set_attributes();
 int tc_rows_per_item();
 cudaError_t gemm_gateup_set_attributes();

@@ -3,14 +3,14 @@
 
 namespace exl3 {
 
-cudaError_t launch_tc_gateup(const GemmArgs &a, int grid, cudaStream_t s)
+cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s)
 {
-    return tc::launch_tc<kModeGateUp>(a, grid, s);
+    return tc::launch_tc<kModeGateUp>(a, maps, grid, s);
 }
 
-cudaError_t launch_tc_down(const GemmArgs &a, int grid, cudaStream_t s)
+cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s)
 {
-    return tc::launch_tc<kModeDown>(a, grid, s);
+    return tc::launch_tc<kModeDown>(a, maps, grid, s);
 }
 
 cudaError_t tc_set_attributes()
