@@ -90,8 +90,9 @@ __device__ __forceinline__ void epi_down_row(const GemmArgs &a, int e, int nbk, 
 
 // The down epilogue in two phases, for kernels that stage many rows and then
 // publish them with a single fence: (1) d = Hb(z)*svh*scale into the staging
-// row; (2) after a __threadfence by every staging thread, count the route and
-// combine the token's block if it was the last one.
+// row (epi_down_stage_row); (2) after a __threadfence by every staging thread,
+// count the routes and combine each token block completed
+// (epi_down_combine_rows).
 __device__ __forceinline__ void epi_down_stage_row(const GemmArgs &a, int e, int nbk, int prow,
                                                    float z[4])
 {
@@ -111,31 +112,45 @@ __device__ __forceinline__ void epi_down_stage_row(const GemmArgs &a, int e, int
         make_float4(z[0], z[1], z[2], z[3]);
 }
 
-__device__ __forceinline__ void epi_down_combine_row(const GemmArgs &a, int nbk, int prow)
+// Counters of many staged rows at once: warp w of nw takes rows w, w + nw, ...
+// (at most 32 per warp), one lane per row, so the atomics are in flight
+// together; each token block that a lane completed is then combined by the
+// whole warp, in lane order.
+__device__ __forceinline__ void epi_down_combine_rows(const GemmArgs &a, int nbk, int row0, int nrows,
+                                                      int w, int nw)
 {
     const int lane = threadIdx.x & 31;
     const int col = nbk * kHb + 4 * lane;
-    const int f = a.packed[prow];
-    const int tok = f / a.topk;
-    int old = 0;
-    if (lane == 0)
-        old = atomicAdd(&a.cnt_comb[tok * a.nb + nbk], 1);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == a.topk - 1) {
-        __threadfence();
-        float o4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < a.topk; j++) {
-            const float w = load_act(a.rw, (size_t)tok * a.topk + j, a.rw_dtype);
-            const float4 d = __ldcg(reinterpret_cast<const float4 *>(
-                a.stage + ((size_t)tok * a.topk + j) * a.out_f + col));
-            o4[0] = __fmaf_rn(w, d.x, o4[0]);
-            o4[1] = __fmaf_rn(w, d.y, o4[1]);
-            o4[2] = __fmaf_rn(w, d.z, o4[2]);
-            o4[3] = __fmaf_rn(w, d.w, o4[3]);
+    for (int base = w; base < nrows; base += 32 * nw) {
+        const int r = base + lane * nw;
+        int tok = -1;
+        if (r < nrows) {
+            const int f = a.packed[row0 + r];
+            const int t = f / a.topk;
+            if (atomicAdd(&a.cnt_comb[t * a.nb + nbk], 1) == a.topk - 1)
+                tok = t;
         }
-        store_act4(a.out, (size_t)tok * a.out_f + col, a.act_dtype, o4);
-        if (lane == 0)
-            a.cnt_comb[tok * a.nb + nbk] = 0;
+        unsigned done = __ballot_sync(0xffffffffu, tok >= 0);
+        if (done)
+            __threadfence();
+        while (done) {
+            const int src = __ffs(done) - 1;
+            done &= done - 1;
+            const int t = __shfl_sync(0xffffffffu, tok, src);
+            float o4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < a.topk; j++) {
+                const float wj = load_act(a.rw, (size_t)t * a.topk + j, a.rw_dtype);
+                const float4 d = __ldcg(reinterpret_cast<const float4 *>(
+                    a.stage + ((size_t)t * a.topk + j) * a.out_f + col));
+                o4[0] = __fmaf_rn(wj, d.x, o4[0]);
+                o4[1] = __fmaf_rn(wj, d.y, o4[1]);
+                o4[2] = __fmaf_rn(wj, d.z, o4[2]);
+                o4[3] = __fmaf_rn(wj, d.w, o4[3]);
+            }
+            store_act4(a.out, (size_t)t * a.out_f + col, a.act_dtype, o4);
+            if (lane == 0)
+                a.cnt_comb[t * a.nb + nbk] = 0;
+        }
     }
 }
 

@@ -10,8 +10,9 @@
 //
 // Work item = (up to 256 routes of one expert, 128-output block); the whole
 // contraction runs in one CTA (one persistent CTA per SM).  Roles:
-//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 4-slot
-//               ring (mbarrier complete_tx) and prefetches later rows to L2;
+//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 6-slot
+//               ring (mbarrier complete_tx) and prefetches later rows (also
+//               the next item's first ones) to L2;
 //   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
 //               256 columns = routes each); lane 0 issues tcgen05.mma
 //               (M=128, N=routes rounded up to 16, K=16) per stage and
@@ -42,7 +43,7 @@ namespace tc {
 
 constexpr int kNT = 256;          // routes per work item (MMA N upper bound)
 constexpr int kStages = 3;        // decoded-weight (A) stages
-constexpr int kTwSlots = 4;       // trellis word slots
+constexpr int kTwSlots = 6;       // trellis word slots
 constexpr int kBRingBytes = 128 * 1024;   // activation (B) stages, sized per item
 constexpr int kMaxBSlots = 16;
 constexpr int kTwAhead = 16;      // trellis stages prefetched into L2 ahead
@@ -65,8 +66,11 @@ struct Traits {
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + kStages * nproj * a_bytes;
     static constexpr int off_tw = off_b + kBRingBytes;
-    static constexpr int off_zs = off_tw + kTwSlots * kTwSlotBytes;
-    static constexpr int off_bar = off_zs + nproj * kEpiRows * kZsLd * 4;
+    // epilogue staging reuses the A ring: it runs after the item's last MMA
+    // and before the next item's first decoded stage
+    static constexpr int off_zs = off_a;
+    static_assert(nproj * kEpiRows * kZsLd * 4 <= kStages * nproj * a_bytes, "staging fits the A ring");
+    static constexpr int off_bar = off_tw + kTwSlots * kTwSlotBytes;
     static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 2;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int total = off_misc + 64;
@@ -84,7 +88,9 @@ struct TcMapsDev {
 // Activation ring geometry of one work item: RB = the item's routes rounded
 // up to a power of two (>= 16), one stage = nproj x KS/8 boxes of RB rows; as
 // many stages as fit in the ring (at most 16).  Items of the same geometry
-// continue one ring; a change of geometry first drains it.
+// continue one ring; a change of geometry first drains it.  (Rounding to a
+// power of two fetches about 5% more rows than rounding to 16 on a Zipf-routed
+// layer, and keeps one box per 8 inputs.)
 struct BGeom {
     int rb, map, proj_bytes, stage_bytes, nslots;
 };
@@ -408,43 +414,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         // ---------------- producer: trellis rows -> word slots
         if (lane == 0) {
             uint32_t g = 0;
-            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-                const TcItem it = tc_item<MODE>(a, item);
+            // trellis rows of one item: first row of each projection's 128-output
+            // block, K per projection, bytes per stage
+            struct Src {
                 const uint32_t *tr[2];
-                int Kp[2];
-                uint32_t bytes = 0;
+                int K[2];
+                uint32_t bytes;
+            };
+            auto src_of = [&](int item) {
+                const TcItem it = tc_item<MODE>(a, item);
+                Src r;
+                r.bytes = 0;
                 for (int p = 0; p < T::nproj; p++) {
                     const int i = it.e * 3 + proj_index<MODE>(p);
-                    tr[p] = reinterpret_cast<const uint32_t *>(a.t_trellis[i]);
-                    Kp[p] = a.t_K[i];
-                    bytes += T::T * 256 * Kp[p];
+                    r.K[p] = a.t_K[i];
+                    r.tr[p] = reinterpret_cast<const uint32_t *>(a.t_trellis[i]) + (size_t)it.nbk * 8 * (8 * r.K[p]);
+                    r.bytes += T::T * 256 * r.K[p];
                 }
-                auto prefetch_stage = [&](int s) {
-                    for (int p = 0; p < T::nproj; p++)
-                        for (int t = 0; t < T::T; t++) {
-                            const int tk = s * T::T + t;
-                            prefetch_l2_bulk(tr[p] + ((size_t)tk * ntn + (size_t)it.nbk * 8) * (8 * Kp[p]),
-                                             256 * Kp[p]);
-                        }
-                };
-                for (int s = 0; s < kTwAhead && s < nst; s++)
-                    prefetch_stage(s);
+                return r;
+            };
+            auto row_of = [&](const Src &r, int p, int tk) { return r.tr[p] + (size_t)tk * ntn * (8 * r.K[p]); };
+            auto prefetch_stage = [&](const Src &r, int s) {
+                for (int p = 0; p < T::nproj; p++)
+                    for (int t = 0; t < T::T; t++)
+                        prefetch_l2_bulk(row_of(r, p, s * T::T + t), 256 * r.K[p]);
+            };
+            int item = blockIdx.x;
+            Src cur = src_of(item);
+            for (int s = 0; s < kTwAhead && s < nst; s++)
+                prefetch_stage(cur, s);
+            for (; item < n_items && !*abort; item += gridDim.x) {
+                const int next = item + (int)gridDim.x;
+                const Src nxt = next < n_items ? src_of(next) : cur;
                 for (int s = 0; s < nst; s++, g++) {
-                    if (s + kTwAhead < nst)
-                        prefetch_stage(s + kTwAhead);
+                    // rows kTwAhead stages ahead, running into the next item
+                    const int sp = s + kTwAhead;
+                    if (sp < nst)
+                        prefetch_stage(cur, sp);
+                    else if (next < n_items && sp - nst < nst)
+                        prefetch_stage(nxt, sp - nst);
                     const int slot = g % kTwSlots;
                     if (g >= kTwSlots &&
                         !wait_bar(&B.twempty[slot], ((g / kTwSlots) - 1) & 1, abort, a.hdr))
                         break;
                     uint8_t *dst = smem + T::off_tw + slot * kTwSlotBytes;
-                    mbar_arrive_expect_tx(&B.twfull[slot], bytes);
+                    mbar_arrive_expect_tx(&B.twfull[slot], cur.bytes);
                     for (int p = 0; p < T::nproj; p++)
-                        for (int t = 0; t < T::T; t++) {
-                            const int tk = s * T::T + t;
-                            const uint32_t *src = tr[p] + ((size_t)tk * ntn + (size_t)it.nbk * 8) * (8 * Kp[p]);
-                            bulk_g2s(dst + (p * T::T + t) * 2048, src, 256 * Kp[p], &B.twfull[slot]);
-                        }
+                        for (int t = 0; t < T::T; t++)
+                            bulk_g2s(dst + (p * T::T + t) * 2048, row_of(cur, p, s * T::T + t),
+                                     256 * cur.K[p], &B.twfull[slot]);
                 }
+                cur = nxt;
             }
         }
     } else if (warp == 1) {
@@ -607,8 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 // all of this item's staged rows, then one fence, then the counters
                 __threadfence();
                 named_barrier(1, kDecThreads);
-                for (int r = dw; r < it.nrows; r += kDecWarps)
-                    epi_down_combine_row(a, it.nbk, it.row0 + r);
+                epi_down_combine_rows(a, it.nbk, it.row0, it.nrows, dw, kDecWarps);
             }
         }
     }
