@@ -92,21 +92,23 @@ EncodeTiledFn encode_tiled()
     return fn;
 }
 
-// fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box height
-// 16 << i rows, box width 8; rows past the end read as zero.
-bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows)
+// fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box {ks, 16 << i}
+// with the swizzle of a ks * 2-byte row (64 or 128 bytes); rows past the end
+// read as zero.
+bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows, int ks)
 {
     EncodeTiledFn fn = encode_tiled();
-    if (fn == nullptr)
+    if (fn == nullptr || (ks != 32 && ks != 64))
         return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = ks == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     for (int i = 0; i < kTcMaps; i++) {
-        const cuuint32_t box[2] = {8, (cuuint32_t)(16 << i)};
+        const cuuint32_t box[2] = {(cuuint32_t)ks, (cuuint32_t)(16 << i)};
         if (fn(&m.act[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
     return true;
@@ -250,7 +252,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
     TcMaps maps1, maps2;
-    if (use_tc && (!encode_act_maps(maps1, g.act, 2 * hidden, R) || !encode_act_maps(maps2, g.ad, inter, R)))
+    if (use_tc && (!encode_act_maps(maps1, g.act, 2 * hidden, R, kTcKsGateUp) ||
+                   !encode_act_maps(maps2, g.ad, inter, R, kTcKsDown)))
         return EXL3_E_CUDA;
     if ((use_tc ? launch_tc_gateup(g, maps1, sms, s) : launch_gemm_gateup(additive, nrb, g, sms * ctas, s)) !=
         cudaSuccess)

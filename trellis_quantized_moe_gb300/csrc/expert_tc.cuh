@@ -29,9 +29,11 @@
 //               ring that runs as far ahead of the MMAs as it has room.
 // A layout (K-major, no swizzle): element (r, k) of a stage tile sits at
 // (r/8)*SBO + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes, SBO = (KS/8)*128.
-// B layout (K-major, no swizzle, as one TMA box {8 inputs, RB rows} per 8
-// inputs): (k/8)*RB*16 + r*16 + (k%8)*2, i.e. core matrices 128 bytes apart
-// along the routes and RB*16 bytes apart along k.
+// B layout (K-major, swizzled; one 2D TMA box {KS inputs, RB rows} per
+// projection and stage): route r's KS inputs are one 2*KS-byte row (64 bytes
+// with the 64-byte swizzle for gate/up, 128 with the 128-byte swizzle for
+// down), 8-row groups 16*KS bytes apart; the swizzle permutes the 16-byte
+// chunks of row r by r % 8 (64-byte: (r / 2) % 4) and is undone by the MMA.
 #pragma once
 #include <string.h>
 #include "common.cuh"
@@ -58,7 +60,7 @@ constexpr int kZsLd = kHb + 4;
 template <int MODE>
 struct Traits {
     static constexpr int nproj = (MODE == kModeGateUp) ? 2 : 1;
-    static constexpr int KS = (MODE == kModeGateUp) ? 32 : 64;   // inputs per stage
+    static constexpr int KS = (MODE == kModeGateUp) ? kTcKsGateUp : kTcKsDown;   // inputs per stage
     static constexpr int T = KS / 16;                            // trellis rows per stage
     static constexpr int SBO = (KS / 8) * 128;
     static constexpr int a_bytes = 128 * KS * 2;                 // per projection
@@ -144,6 +146,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;                              // tcgen05 descriptor version
     return d;                                            // no swizzle
+}
+
+// swizzled K-major operand (rows of 64 or 128 bytes): sbo = bytes between
+// 8-row groups; the k offset inside the row is added to the start address
+__device__ __forceinline__ uint64_t smem_desc_swz(uint32_t addr, uint32_t sbo, int row_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;                              // unused for swizzled K-major
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;                              // tcgen05 descriptor version
+    d |= (uint64_t)(row_bytes == 128 ? 2 : 4) << 61;     // 128-byte / 64-byte swizzle
+    return d;
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -498,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
 #pragma unroll
                         for (int ks = 0; ks < T::KS / 16; ks++)
                             mma_f16(tmem + p * kNT, smem_desc(abase + ks * 256, 128, T::SBO),
-                                    smem_desc(bbase + ks * 32 * bg.rb, 16 * bg.rb, 128), idesc,
+                                    smem_desc_swz(bbase + ks * 32, 16 * T::KS, 2 * T::KS), idesc,
                                     (s > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&B.empty[slot]);
@@ -541,10 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                     uint8_t *dst = smem + T::off_b + bs * bg.stage_bytes;
                     mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
                     for (int p = 0; p < T::nproj; p++)
-#pragma unroll
-                        for (int kc = 0; kc < T::KS / 8; kc++)
-                            tma_load_2d(dst + p * bg.proj_bytes + kc * 16 * bg.rb, map,
-                                        p * a.in_f + s * T::KS + kc * 8, it.row0, &B.bfull[bs]);
+                        tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
+                                    &B.bfull[bs]);
                 }
             }
             // every load this thread issued is consumed by an MMA before the

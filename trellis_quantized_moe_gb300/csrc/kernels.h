@@ -90,9 +90,13 @@ cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s);
 cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
-// Prefill-regime activation tensor maps: a 2D fp16 [rows][cols] view of the
-// rotated activations, one map per TMA box height 16 << i rows (box width 8).
+// Prefill-regime activation tensor maps: 2D fp16 [rows][cols] views of the
+// rotated activations, one map per box height 16 << i rows; a box {KS, 16 << i}
+// (swizzled: 64-byte rows for KS = 32, 128-byte rows for KS = 64) is one
+// stage's B tile of one projection.  Inputs per stage: gate/up 32, down 64.
 constexpr int kTcMaps = 5;
+constexpr int kTcKsGateUp = 32;
+constexpr int kTcKsDown = 64;
 struct TcMaps {
     CUtensorMap act[kTcMaps];
 };
