@@ -303,6 +303,22 @@ struct TcItem {
     int e, row0, nrows, nbk;
 };
 
+// Position in a ring of N slots: the slot and the parity of its current use
+// (flips whenever the slot index wraps).  A consumer waits for parity `phase`
+// on a slot's full barrier; a producer waits for `phase ^ 1` on its empty
+// barrier, which a freshly initialised barrier already satisfies.
+template <int N>
+struct RingPos {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
+
 template <int MODE>
 __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 {
@@ -324,21 +340,22 @@ __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? 
 // compile-time.
 template <int MODE, int K, int CB>
 __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
-                                          volatile int *abort, const TcItem &it, uint32_t &g,
-                                          int p, int t, int m)
+                                          volatile int *abort, const TcItem &it,
+                                          RingPos<kStages> &ra, RingPos<kTwSlots> &rt, int p, int t,
+                                          int m)
 {
     using T = Traits<MODE>;
     const int nst = a.in_f / T::KS;
     const ColumnWindow<K> cw(m & 15);
     const int tile_off = (p * T::T + t) * 2048 + (m >> 4) * 32 * K;          // bytes
     const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
-    for (int s = 0; s < nst; s++, g++) {
-        const int slot = g % kStages;
-        const int tws = g % kTwSlots;
-        // the A slot is free once the MMA of stage g - 3 completed
-        if (g >= kStages && !wait_bar(&B.empty[slot], ((g / kStages) - 1) & 1, abort, a.hdr))
+    for (int s = 0; s < nst; s++, ra.next(), rt.next()) {
+        const int slot = ra.slot;
+        const int tws = rt.slot;
+        // the A slot is free once the MMA of its previous stage completed
+        if (!wait_bar(&B.empty[slot], ra.phase ^ 1, abort, a.hdr))
             return false;
-        if (!wait_bar(&B.twfull[tws], (g / kTwSlots) & 1, abort, a.hdr))
+        if (!wait_bar(&B.twfull[tws], rt.phase, abort, a.hdr))
             return false;
         uint32_t w[8];
         decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + tws * kTwSlotBytes +
@@ -356,14 +373,15 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
 
 template <int MODE, int K>
 __device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t *smem, const Bars &B,
-                                             volatile int *abort, const TcItem &it, uint32_t &g,
-                                             int p, int t, int m)
+                                             volatile int *abort, const TcItem &it,
+                                             RingPos<kStages> &ra, RingPos<kTwSlots> &rt, int p,
+                                             int t, int m)
 {
     if (cb == EXL3_CB_MUL1)
-        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, g, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, ra, rt, p, t, m);
     if (cb == EXL3_CB_3INST)
-        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, g, p, t, m);
-    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, g, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, ra, rt, p, t, m);
+    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, ra, rt, p, t, m);
 }
 
 template <int MODE>
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     if (warp == 0) {
         // ---------------- producer: trellis rows -> word slots
         if (lane == 0) {
-            uint32_t g = 0;
+            RingPos<kTwSlots> rt;
             // trellis rows of one item: first row of each projection's 128-output
             // block, K per projection, bytes per stage
             struct Src {
@@ -461,16 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             for (; item < n_items && !*abort; item += gridDim.x) {
                 const int next = item + (int)gridDim.x;
                 const Src nxt = next < n_items ? src_of(next) : cur;
-                for (int s = 0; s < nst; s++, g++) {
+                for (int s = 0; s < nst; s++, rt.next()) {
                     // rows kTwAhead stages ahead, running into the next item
                     const int sp = s + kTwAhead;
                     if (sp < nst)
                         prefetch_stage(cur, sp);
                     else if (next < n_items && sp - nst < nst)
                         prefetch_stage(nxt, sp - nst);
-                    const int slot = g % kTwSlots;
-                    if (g >= kTwSlots &&
-                        !wait_bar(&B.twempty[slot], ((g / kTwSlots) - 1) & 1, abort, a.hdr))
+                    const int slot = rt.slot;
+                    if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
                         break;
                     uint8_t *dst = smem + T::off_tw + slot * kTwSlotBytes;
                     mbar_arrive_expect_tx(&B.twfull[slot], cur.bytes);
@@ -485,39 +502,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            uint32_t g = 0, nit = 0, bphase = 0;     // bphase: parity bit per B slot
-            int gb = 0, cur_rb = 0;                   // B ring position, geometry
+            RingPos<kStages> ra;
+            uint32_t nit = 0, bphase = 0;            // bphase: parity bit per B slot
+            int bs = 0, cur_rb = 0;                   // B ring slot, geometry
+            // descriptors of A slot 0 / B ring byte 0; offsets are added in
+            // 16-byte units to the address field
+            const uint64_t adesc0 = smem_desc(smem_addr(smem + T::off_a), 128, T::SBO);
+            const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + T::off_b), 16 * T::KS, 2 * T::KS);
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
                 const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
                 if (bg.rb != cur_rb) {
-                    gb = 0;
+                    bs = 0;
                     cur_rb = bg.rb;
                 }
+                const uint32_t bproj16 = bg.proj_bytes >> 4, bstage16 = bg.stage_bytes >> 4;
                 const int n_mma = max(16, (it.nrows + 15) & ~15);
                 const uint32_t idesc = instr_desc(n_mma);
                 if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
                     break;
                 fence_after();
-                for (int s = 0; s < nst; s++, g++, gb++) {
-                    const int slot = g % kStages;
-                    const int bs = gb % bg.nslots;
-                    if (!wait_bar(&B.full[slot], (g / kStages) & 1, abort, a.hdr) ||
+                for (int s = 0; s < nst; s++, ra.next()) {
+                    const int slot = ra.slot;
+                    if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
                         !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
                         break;
                     bphase ^= 1u << bs;
                     fence_after();
-                    for (int p = 0; p < T::nproj; p++) {
-                        const uint32_t abase = smem_addr(smem + T::off_a + (slot * T::nproj + p) * T::a_bytes);
-                        const uint32_t bbase = smem_addr(smem + T::off_b + bs * bg.stage_bytes + p * bg.proj_bytes);
+                    const uint64_t ad = adesc0 + (uint32_t)(slot * (T::nproj * T::a_bytes >> 4));
+                    const uint64_t bd = bdesc0 + (uint32_t)(bs * bstage16);
+#pragma unroll
+                    for (int p = 0; p < T::nproj; p++)
 #pragma unroll
                         for (int ks = 0; ks < T::KS / 16; ks++)
-                            mma_f16(tmem + p * kNT, smem_desc(abase + ks * 256, 128, T::SBO),
-                                    smem_desc_swz(bbase + ks * 32, 16 * T::KS, 2 * T::KS), idesc,
+                            mma_f16(tmem + p * kNT, ad + (uint32_t)(p * (T::a_bytes >> 4) + ks * 16),
+                                    bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
                                     (s > 0 || ks > 0) ? 1u : 0u);
-                    }
                     mma_commit(&B.empty[slot]);
                     mma_commit(&B.bempty[bs]);
+                    if (++bs == bg.nslots)
+                        bs = 0;
                 }
                 mma_commit(B.accfull);
             }
@@ -526,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         // ---------------- activation producer: 2D TMA boxes into the B ring
         if (lane == 0) {
             uint32_t pend = 0, ph = 0;                // per B slot: use in flight, parity
-            int gb = 0, cur_rb = 0;
+            int bs = 0, cur_rb = 0;
             auto reclaim = [&](int bs) -> bool {
                 if ((pend >> bs) & 1) {
                     if (!wait_bar(&B.bempty[bs], (ph >> bs) & 1, abort, a.hdr))
@@ -544,12 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                     // slots of the old geometry overlap the new ones: drain the ring
                     for (int bs = 0; ok && bs < kMaxBSlots; bs++)
                         ok = reclaim(bs);
-                    gb = 0;
+                    bs = 0;
                     cur_rb = bg.rb;
                 }
                 const CUtensorMap *map = &maps.act[bg.map];
-                for (int s = 0; ok && s < nst; s++, gb++) {
-                    const int bs = gb % bg.nslots;
+                for (int s = 0; ok && s < nst; s++, bs = (bs + 1 == bg.nslots) ? 0 : bs + 1) {
                     if (!(ok = reclaim(bs)))
                         break;
                     pend |= 1u << bs;
@@ -571,21 +594,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         const int t = (MODE == kModeGateUp) ? ((dt >> 7) & 1) : (dt >> 7);
         const int m = dt & 127;
         float *zs = reinterpret_cast<float *>(smem + T::off_zs);
-        uint32_t g = 0, nit = 0;
+        RingPos<kStages> ra;
+        RingPos<kTwSlots> rt;
+        uint32_t nit = 0;
         for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
             const TcItem it = tc_item<MODE>(a, item);
             const int pi = it.e * 3 + proj_index<MODE>(p);
             const int K = a.t_K[pi], cb = a.t_cb[pi];
             bool ok;
             switch (K) {
-                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, g, p, t, m); break;
-                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, g, p, t, m); break;
+                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
             }
             if (!ok || *abort)
                 break;
