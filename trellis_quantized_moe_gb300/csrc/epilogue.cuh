@@ -11,36 +11,67 @@
 
 namespace exl3 {
 
+// Per-column factors of one (expert, 128-output block), lane l holding
+// outputs 4l..4l+3: they depend on neither the route nor the row, so a kernel
+// that runs many rows of one block loads them once.
+struct GateUpConsts {
+    float svg[4], scg[4], svu[4], scu[4], sud[4];
+};
+
+__device__ __forceinline__ void epi_gateup_consts(const GemmArgs &a, int e, int nbk, GateUpConsts &c)
+{
+    const int col = nbk * kHb + 4 * (threadIdx.x & 31);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 0]), col, c.svg);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 0]), col, c.scg);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 1]), col, c.svu);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 1]), col, c.scu);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + 2]), col, c.sud);
+}
+
 // gate/up: g' = Hb(g)*svh*scale, u' likewise, h = silu(g')*u', then the down
 // projection's input rotation a_d = Hb(h * suh_down) over the same 128 block of
 // the intermediate dimension; stored as the fp16 MMA operand of the down GEMM.
-__device__ __forceinline__ void epi_gateup_row(const GemmArgs &a, int e, int nbk, int prow,
-                                               float gv[4], float uv[4])
+__device__ __forceinline__ void epi_gateup_row(const GemmArgs &a, const GateUpConsts &c, int nbk,
+                                               int prow, float gv[4], float uv[4])
 {
     const int lane = threadIdx.x & 31;
     const int col = nbk * kHb + 4 * lane;
-    float sv[4], sc[4], h[4];
+    float h[4];
     warp_hadamard128(gv);
     warp_hadamard128(uv);
-    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 0]), col, sv);
-    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 0]), col, sc);
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        gv[i] = gv[i] * kInvSqrt128 * sv[i] * sc[i];
-    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 1]), col, sv);
-    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 1]), col, sc);
+        gv[i] = gv[i] * kInvSqrt128 * c.svg[i] * c.scg[i];
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        uv[i] = uv[i] * kInvSqrt128 * sv[i] * sc[i];
-    load_half4(reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + 2]), col, sv);
+        uv[i] = uv[i] * kInvSqrt128 * c.svu[i] * c.scu[i];
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        h[i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i] * sv[i];
+        h[i] = gv[i] / (1.0f + expf(-gv[i])) * uv[i] * c.sud[i];
     warp_hadamard128(h);
 #pragma unroll
     for (int i = 0; i < 4; i++)
         h[i] *= kInvSqrt128;
     store_act4(a.ad, (size_t)prow * a.out_f + col, EXL3_F16, h);
+}
+
+__device__ __forceinline__ void epi_gateup_row(const GemmArgs &a, int e, int nbk, int prow,
+                                               float gv[4], float uv[4])
+{
+    GateUpConsts c;
+    epi_gateup_consts(a, e, nbk, c);
+    epi_gateup_row(a, c, nbk, prow, gv, uv);
+}
+
+struct DownConsts {
+    float sv[4], sc[4];
+};
+
+__device__ __forceinline__ void epi_down_consts(const GemmArgs &a, int e, int nbk, DownConsts &c)
+{
+    const int col = nbk * kHb + 4 * (threadIdx.x & 31);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 2]), col, c.sv);
+    load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 2]), col, c.sc);
 }
 
 // down: d = Hb(z)*svh*scale into the fp32 staging row of flat route f; the
@@ -93,20 +124,15 @@ __device__ __forceinline__ void epi_down_row(const GemmArgs &a, int e, int nbk, 
 // row (epi_down_stage_row); (2) after a __threadfence by every staging thread,
 // count the routes and combine each token block completed
 // (epi_down_combine_rows).
-__device__ __forceinline__ void epi_down_stage_row(const GemmArgs &a, int e, int nbk, int prow,
-                                                   float z[4])
+__device__ __forceinline__ void epi_down_stage_row(const GemmArgs &a, const DownConsts &c, int nbk,
+                                                   int prow, float z[4])
 {
     const int lane = threadIdx.x & 31;
     const int col = nbk * kHb + 4 * lane;
-    const uint16_t *svh = reinterpret_cast<const uint16_t *>(a.t_svh[e * 3 + 2]);
-    const uint16_t *scl = reinterpret_cast<const uint16_t *>(a.t_scale[e * 3 + 2]);
-    float sv[4], sc[4];
     warp_hadamard128(z);
-    load_half4(svh, col, sv);
-    load_half4(scl, col, sc);
 #pragma unroll
     for (int i = 0; i < 4; i++)
-        z[i] = z[i] * kInvSqrt128 * sv[i] * sc[i];
+        z[i] = z[i] * kInvSqrt128 * c.sv[i] * c.sc[i];
     const int f = a.packed[prow];
     *reinterpret_cast<float4 *>(a.stage + (size_t)f * a.out_f + col) =
         make_float4(z[0], z[1], z[2], z[3]);

@@ -54,7 +54,7 @@ constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kBWarp = 2 + kDecWarps;     // activation producer
 constexpr int kThreads = kDecThreads + 96;
-constexpr int kEpiRows = 16;
+constexpr int kEpiRows = 32;      // routes per epilogue interval (2 per decode warp)
 constexpr int kZsLd = kHb + 4;
 
 template <int MODE>
@@ -203,12 +203,19 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
 template <int NREG>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NREG])
 {
-    if (NREG == 8) {
+    if constexpr (NREG == 16) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                       "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                       "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                     : "r"(taddr));
+    } else if constexpr (NREG == 8) {
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
                        "=r"(v[6]), "=r"(v[7])
                      : "r"(taddr));
     } else {
+        static_assert(NREG == 4, "tcgen05.ld width");
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
                      : "r"(taddr));
@@ -614,47 +621,58 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             }
             if (!ok || *abort)
                 break;
-            // ---- epilogue: TMEM -> shared (16 routes at a time) -> per-row epilogue
+            // ---- epilogue: TMEM -> shared (32 routes at a time) -> per-row epilogue
             if (!wait_bar(B.accfull, nit & 1, abort, a.hdr))
                 break;
             fence_after();
             const int q = (warp & 3);                 // TMEM lane quarter of this warp
+            GateUpConsts cg;
+            DownConsts cd;
+            if (MODE == kModeGateUp)
+                epi_gateup_consts(a, it.e, it.nbk, cg);
+            else
+                epi_down_consts(a, it.e, it.nbk, cd);
             float fac[2];
             for (int pp = 0; pp < T::nproj; pp++)
                 fac[pp] = (a.t_cb[it.e * 3 + proj_index<MODE>(pp)] == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+            // the four warps of a lane quarter split the interval's columns
+            const int jq = dw >> 2;
             for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
                 if (MODE == kModeGateUp) {
-                    const int pp = dw >> 3, half = (dw & 7) >> 2;
+                    const int pp = jq >> 1, half = jq & 1;
+                    uint32_t v[16];
+                    tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + pp * kNT + r0 + half * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 16; j++)
+                        zs[(pp * kEpiRows + half * 16 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[pp];
+                } else {
                     uint32_t v[8];
-                    tmem_ld<8>(tmem + ((uint32_t)(32 * q) << 16) + pp * kNT + r0 + half * 8, v);
+                    tmem_ld<8>(tmem + ((uint32_t)(32 * q) << 16) + r0 + jq * 8, v);
 #pragma unroll
                     for (int j = 0; j < 8; j++)
-                        zs[(pp * kEpiRows + half * 8 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[pp];
-                } else {
-                    const int cq = dw >> 2;
-                    uint32_t v[4];
-                    tmem_ld<4>(tmem + ((uint32_t)(32 * q) << 16) + r0 + cq * 4, v);
-#pragma unroll
-                    for (int j = 0; j < 4; j++)
-                        zs[(cq * 4 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[0];
+                        zs[(jq * 8 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[0];
                 }
                 named_barrier(1, kDecThreads);
-                const int r = r0 + dw;
-                if (r < it.nrows) {
-                    if (MODE == kModeGateUp) {
-                        float gv[4], uv[4];
+                // rows r0 + dw and r0 + dw + 16 of this warp
 #pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            gv[i] = zs[dw * kZsLd + 4 * lane + i];
-                            uv[i] = zs[(kEpiRows + dw) * kZsLd + 4 * lane + i];
+                for (int h = 0; h < 2; h++) {
+                    const int rr = dw + 16 * h, r = r0 + rr;
+                    if (r < it.nrows) {
+                        if (MODE == kModeGateUp) {
+                            float gv[4], uv[4];
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                gv[i] = zs[rr * kZsLd + 4 * lane + i];
+                                uv[i] = zs[(kEpiRows + rr) * kZsLd + 4 * lane + i];
+                            }
+                            epi_gateup_row(a, cg, it.nbk, it.row0 + r, gv, uv);
+                        } else {
+                            float z[4];
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                z[i] = zs[rr * kZsLd + 4 * lane + i];
+                            epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
                         }
-                        epi_gateup_row(a, it.e, it.nbk, it.row0 + r, gv, uv);
-                    } else {
-                        float z[4];
-#pragma unroll
-                        for (int i = 0; i < 4; i++)
-                            z[i] = zs[dw * kZsLd + 4 * lane + i];
-                        epi_down_stage_row(a, it.e, it.nbk, it.row0 + r, z);
                     }
                 }
                 named_barrier(1, kDecThreads);
