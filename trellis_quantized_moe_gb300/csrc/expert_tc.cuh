@@ -10,9 +10,10 @@
 //
 // Work item = (up to 256 routes of one expert, 128-output block); the whole
 // contraction runs in one CTA (one persistent CTA per SM).  Roles:
-//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 6-slot
-//               ring (mbarrier complete_tx) and prefetches later rows (also
-//               the next item's first ones) to L2;
+//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 48 KB
+//               ring of stage slots sized by the layer's largest K (6 slots at
+//               K = 8, 12 at K = 4, 16 at K <= 3), mbarrier complete_tx, and
+//               prefetches later rows (also the next item's first ones) to L2;
 //   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
 //               256 columns = routes each); lane 0 issues tcgen05.mma
 //               (M=128, N=routes rounded up to 16, K=16) per stage and
@@ -45,11 +46,11 @@ namespace tc {
 
 constexpr int kNT = 256;          // routes per work item (MMA N upper bound)
 constexpr int kStages = 3;        // decoded-weight (A) stages
-constexpr int kTwSlots = 6;       // trellis word slots
+constexpr int kTwSlots = 16;      // trellis word slots (at most; sized by the layer's largest K)
 constexpr int kBRingBytes = 128 * 1024;   // activation (B) stages, sized per item
 constexpr int kMaxBSlots = 16;
 constexpr int kTwAhead = 16;      // trellis stages prefetched into L2 ahead
-constexpr int kTwSlotBytes = 8192;
+constexpr int kTwRingBytes = 48 * 1024;
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kBWarp = 2 + kDecWarps;     // activation producer
@@ -72,7 +73,7 @@ struct Traits {
     // and before the next item's first decoded stage
     static constexpr int off_zs = off_a;
     static_assert(nproj * kEpiRows * kZsLd * 4 <= kStages * nproj * a_bytes, "staging fits the A ring");
-    static constexpr int off_bar = off_tw + kTwSlots * kTwSlotBytes;
+    static constexpr int off_bar = off_tw + kTwRingBytes;
     static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 2;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int total = off_misc + 64;
@@ -111,15 +112,31 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     return g;
 }
 
+// try_wait with a long suspend-time hint: a waiting thread sleeps until the
+// phase completes (or 1 ms passes) instead of re-polling, which leaves the
+// issue slots of its SM sub-partition to the decode warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
 // as soon as another thread has given up, and then reports false.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
                                          int32_t *hdr)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_try_wait_sleep(bar, parity))
         return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (*abort)
             return false;
         if (clock64() - t0 > (1ll << 31)) {
@@ -326,6 +343,33 @@ struct RingPos {
     }
 };
 
+// The same for a ring whose slot count is known at run time.
+struct RingPosN {
+    uint32_t slot = 0, phase = 0, n = 1;
+    __device__ __forceinline__ void next()
+    {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+// Trellis ring geometry: one slot holds a stage's nproj * T trellis rows
+// (4 rows in both modes), each 256 * kmax bytes.
+struct TwGeom {
+    int row_bytes, slot_bytes, nslots;
+};
+
+__device__ __forceinline__ TwGeom tw_geom(int kmax)
+{
+    TwGeom g;
+    g.row_bytes = 256 * kmax;
+    g.slot_bytes = 4 * g.row_bytes;
+    g.nslots = min(kTwSlots, kTwRingBytes / g.slot_bytes);
+    return g;
+}
+
 template <int MODE>
 __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 {
@@ -348,32 +392,51 @@ __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? 
 template <int MODE, int K, int CB>
 __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
                                           volatile int *abort, const TcItem &it,
-                                          RingPos<kStages> &ra, RingPos<kTwSlots> &rt, int p, int t,
-                                          int m)
+                                          RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
+                                          int p, int t, int m)
 {
     using T = Traits<MODE>;
     const int nst = a.in_f / T::KS;
     const ColumnWindow<K> cw(m & 15);
-    const int tile_off = (p * T::T + t) * 2048 + (m >> 4) * 32 * K;          // bytes
+    const int tile_off = (p * T::T + t) * tg.row_bytes + (m >> 4) * 32 * K;          // bytes
     const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
-    for (int s = 0; s < nst; s++, ra.next(), rt.next()) {
-        const int slot = ra.slot;
-        const int tws = rt.slot;
-        // the A slot is free once the MMA of its previous stage completed
-        if (!wait_bar(&B.empty[slot], ra.phase ^ 1, abort, a.hdr))
+    // two stages per pass (the stage count is even): twice the independent
+    // decode work between barrier operations
+    for (int s = 0; s < nst; s += 2) {
+        RingPos<kStages> ra1 = ra;
+        RingPosN rt1 = rt;
+        ra1.next();
+        rt1.next();
+        if (!wait_bar(&B.twfull[rt.slot], rt.phase, abort, a.hdr) ||
+            !wait_bar(&B.twfull[rt1.slot], rt1.phase, abort, a.hdr))
             return false;
-        if (!wait_bar(&B.twfull[tws], rt.phase, abort, a.hdr))
-            return false;
-        uint32_t w[8];
-        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + tws * kTwSlotBytes +
+        uint32_t w0[8], w1[8];
+        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt.slot * tg.slot_bytes +
                                                                 tile_off),
-                             cw, w);
-        warp_arrive(&B.twempty[tws]);
-        uint8_t *abuf = smem + T::off_a + slot * T::nproj * T::a_bytes + a_off;
-        *reinterpret_cast<uint4 *>(abuf) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4 *>(abuf + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                             cw, w0);
+        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt1.slot * tg.slot_bytes +
+                                                                tile_off),
+                             cw, w1);
+        warp_arrive(&B.twempty[rt.slot]);
+        warp_arrive(&B.twempty[rt1.slot]);
+        // an A slot is free once the MMA of its previous stage completed; the
+        // decode above does not need it
+        if (!wait_bar(&B.empty[ra.slot], ra.phase ^ 1, abort, a.hdr) ||
+            !wait_bar(&B.empty[ra1.slot], ra1.phase ^ 1, abort, a.hdr))
+            return false;
+        uint8_t *abuf0 = smem + T::off_a + ra.slot * T::nproj * T::a_bytes + a_off;
+        uint8_t *abuf1 = smem + T::off_a + ra1.slot * T::nproj * T::a_bytes + a_off;
+        *reinterpret_cast<uint4 *>(abuf0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4 *>(abuf0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+        *reinterpret_cast<uint4 *>(abuf1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        *reinterpret_cast<uint4 *>(abuf1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        warp_arrive(&B.full[slot]);
+        warp_arrive(&B.full[ra.slot]);
+        warp_arrive(&B.full[ra1.slot]);
+        ra1.next();
+        rt1.next();
+        ra = ra1;
+        rt = rt1;
     }
     return true;
 }
@@ -381,14 +444,14 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
 template <int MODE, int K>
 __device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t *smem, const Bars &B,
                                              volatile int *abort, const TcItem &it,
-                                             RingPos<kStages> &ra, RingPos<kTwSlots> &rt, int p,
-                                             int t, int m)
+                                             RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
+                                             int p, int t, int m)
 {
     if (cb == EXL3_CB_MUL1)
-        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, ra, rt, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
     if (cb == EXL3_CB_3INST)
-        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, ra, rt, p, t, m);
-    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, ra, rt, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
+    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
 }
 
 template <int MODE>
@@ -409,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     B.accempty = B.accfull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::off_misc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
+    int *kmax_slot = reinterpret_cast<int *>(smem + T::off_misc + 16);
 
     const int n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
     if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
@@ -440,6 +504,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         *abort = 0;
         fence_mbar_init();
     }
+    if (warp == 0) {
+        // the largest K of this kernel's projections sizes the trellis slots
+        int km = 1;
+        for (int e = lane; e < a.E; e += 32)
+            for (int p = 0; p < T::nproj; p++)
+                km = max(km, min(8, a.t_K[e * 3 + proj_index<MODE>(p)]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            km = max(km, __shfl_xor_sync(0xffffffffu, km, o));
+        if (lane == 0)
+            *kmax_slot = km;
+    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_addr(tmem_slot)), "r"(T::nproj * kNT) : "memory");
@@ -449,11 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    const TwGeom tg = tw_geom(*kmax_slot);
 
     if (warp == 0) {
         // ---------------- producer: trellis rows -> word slots
         if (lane == 0) {
-            RingPos<kTwSlots> rt;
+            RingPosN rt;
+            rt.n = tg.nslots;
             // trellis rows of one item: first row of each projection's 128-output
             // block, K per projection, bytes per stage
             struct Src {
@@ -496,11 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                     const int slot = rt.slot;
                     if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
                         break;
-                    uint8_t *dst = smem + T::off_tw + slot * kTwSlotBytes;
+                    uint8_t *dst = smem + T::off_tw + slot * tg.slot_bytes;
                     mbar_arrive_expect_tx(&B.twfull[slot], cur.bytes);
                     for (int p = 0; p < T::nproj; p++)
                         for (int t = 0; t < T::T; t++)
-                            bulk_g2s(dst + (p * T::T + t) * 2048, row_of(cur, p, s * T::T + t),
+                            bulk_g2s(dst + (p * T::T + t) * tg.row_bytes, row_of(cur, p, s * T::T + t),
                                      256 * cur.K[p], &B.twfull[slot]);
                 }
                 cur = nxt;
@@ -602,7 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         const int m = dt & 127;
         float *zs = reinterpret_cast<float *>(smem + T::off_zs);
         RingPos<kStages> ra;
-        RingPos<kTwSlots> rt;
+        RingPosN rt;
+        rt.n = tg.nslots;
         uint32_t nit = 0;
         for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
             const TcItem it = tc_item<MODE>(a, item);
@@ -610,14 +689,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             const int K = a.t_K[pi], cb = a.t_cb[pi];
             bool ok;
             switch (K) {
-                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
-                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, ra, rt, p, t, m); break;
+                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
             }
             if (!ok || *abort)
                 break;
