@@ -136,6 +136,11 @@ def _stages(w):
     return X.DeviceStages(w.residual, w.alpha, s.residual_K, s.E)
 
 
+# regime of the last run_layer call: workspace header word 8, written by the
+# route-pack kernel (0 = decode-regime kernels ran, 1 = tcgen05 kernels ran)
+LAST = {}
+
+
 def run_layer(w, experts, capacity=None, stages=None, ws=None):
     s = w.spec
     x, ids, rw = moe_inputs(w)
@@ -150,6 +155,7 @@ def run_layer(w, experts, capacity=None, stages=None, ws=None):
         X.exl3_moe_additive(x, ids, rw, experts, stages, cap, ws, out)
     torch.cuda.synchronize()
     assert X.exl3_workspace_error(ws) == 0
+    LAST["regime"] = int(ws[:64 * 4].view(torch.int32)[8].item())
     return out
 
 
@@ -203,6 +209,7 @@ def test_prefill_path_small_layer_full_parity(M, act):
     ex = X.DeviceExperts.from_workload(w)
     assert np.bincount(w.ids.reshape(-1), minlength=8).max() > (256 if M > 1000 else 64)
     out = to_f64(run_layer(w, ex))
+    assert LAST["regime"] == 1
     # outputs are O(1) here (8 experts, top-2): worst element within one output
     # ulp plus 1e-2 of the output rms, rel-L2 2e-3
     assert_close_linear(out, oracle_rows(w), act, f"prefill path M={M}")
@@ -212,8 +219,22 @@ def test_prefill_path_rows_do_not_depend_on_capacity():
     w = _small_layer(600, "f16", seed=7)
     ex = X.DeviceExperts.from_workload(w)
     a = run_layer(w, ex, capacity=512).view(torch.int16).cpu().numpy()
+    assert LAST["regime"] == 1
     b = run_layer(w, ex, capacity=97).view(torch.int16).cpu().numpy()
+    assert LAST["regime"] == 1
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("cfg,M,regime", [(1, 136, 0), (3, 160, 1)])
+def test_regime_choice_above_128_tokens(cfg, M, regime):
+    # both kernel pairs are launched above 128 tokens; the route-pack kernel
+    # picks one from the route counts: few routes per expert (uniform routing)
+    # keep the decode regime, Zipf-concentrated routing takes the tcgen05 path
+    w = MoEWorkload(config(cfg, M=M))
+    out = to_f64(run_layer(w, _experts(cfg)))
+    assert LAST["regime"] == regime
+    rows = np.array([0, M // 2, M - 1])
+    assert_close(out[rows], oracle_rows(w, tokens=rows), f"config {cfg} M={M}")
 
 
 def test_mixed_width_layer_parity():
@@ -226,6 +247,7 @@ def test_mixed_width_layer_parity():
 def test_prefill_layer_parity_sampled():
     w = MoEWorkload(config(3))
     out = to_f64(run_layer(w, _experts(3)))
+    assert LAST["regime"] == 1
     rows = np.array([0, 1500, 3071])
     assert_close(out[rows], oracle_rows(w, tokens=rows), "config 3")
     assert np.all(np.isfinite(out))

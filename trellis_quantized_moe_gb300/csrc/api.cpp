@@ -159,14 +159,18 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     uint8_t *w = static_cast<uint8_t *>(ws);
     int32_t *hdr = reinterpret_cast<int32_t *>(w + L.hdr);
     const int R = L.R;
-    // Prefill regime (tcgen05, up to 256 routes per item): more than 128 tokens,
-    // no residual stages and spans of more than 64 routes per expert on
-    // average.  Otherwise the decode regime (mma.sync): 16-row items (1 CTA/SM)
-    // when experts carry more than 8 routes on average, else 8 rows.  M <= 128
-    // always takes the decode regime, so a row's bytes never depend on M there.
+    // Two regimes: decode (mma.sync; 16-row items at 1 CTA/SM when experts
+    // carry more than 8 routes on average, else 8 rows; residual stages: 8
+    // rows) and prefill (tcgen05, up to 256 routes per item, no stages).  With
+    // more than 128 tokens both kernel pairs are launched and the route-pack
+    // kernel picks one from the per-expert route counts (the other pair
+    // returns at once); stages with a nonzero scale force the decode regime.
+    // M <= 128 always takes the decode regime, so a row's bytes never depend
+    // on M there.
     const int active = E < R ? E : R;
-    const bool use_tc = !additive && M > 128 && (long long)R > 64LL * active;
-    const int nrb = additive ? 1 : (R > 8 * active ? 2 : 1);
+    const bool tc_ok = M > 128;
+    const int nrb_plain = R > 8 * active ? 2 : 1;
+    const int nrb = additive ? 1 : nrb_plain;
     const int ctas = gemm_ctas_per_sm(nrb, additive);
 
     RoutePackArgs rp{};
@@ -174,7 +178,10 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.R = R;
     rp.E = E;
     rp.capacity = capacity;
-    rp.rg_size = use_tc ? tc_rows_per_item() : 8 * nrb;
+    rp.rg_size = 8 * nrb;
+    rp.tc_rows = tc_ok ? tc_rows_per_item() : 0;
+    rp.cost_rg = 8 * nrb_plain;
+    rp.dec_unit_cost = nrb_plain == 2 ? 1700 : 1050;
     rp.nw = route_pack_hist_warps(E);
     rp.offsets = reinterpret_cast<int32_t *>(w + L.offsets);
     rp.packed = reinterpret_cast<int32_t *>(w + L.packed);
@@ -184,8 +191,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.rg = w + L.rg;
     rp.nb1 = L.nb1;
     rp.nb2 = L.nb2;
-    rp.nchunks1 = use_tc ? 1 : L.nchunks1;     // the prefill path never splits chunks
-    rp.nchunks2 = use_tc ? 1 : L.nchunks2;
+    rp.nchunks1 = L.nchunks1;
+    rp.nchunks2 = L.nchunks2;
     rp.split_pairs1 = L.split_pairs1;
     rp.split_pairs2 = L.split_pairs2;
     rp.num_sms = sms;
@@ -252,11 +259,11 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
     TcMaps maps1, maps2;
-    if (use_tc && (!encode_act_maps(maps1, g.act, 2 * hidden, R, kTcKsGateUp) ||
-                   !encode_act_maps(maps2, g.ad, inter, R, kTcKsDown)))
+    if (tc_ok && (!encode_act_maps(maps1, g.act, 2 * hidden, R, kTcKsGateUp) ||
+                  !encode_act_maps(maps2, g.ad, inter, R, kTcKsDown)))
         return EXL3_E_CUDA;
-    if ((use_tc ? launch_tc_gateup(g, maps1, sms, s) : launch_gemm_gateup(additive, nrb, g, sms * ctas, s)) !=
-        cudaSuccess)
+    if ((tc_ok && launch_tc_gateup(g, maps1, sms, s) != cudaSuccess) ||
+        launch_gemm_gateup(additive, nrb, g, sms * ctas, s) != cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(3, s);
 
@@ -275,8 +282,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.rw_dtype = rw_dtype;
     g.cnt_comb = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = out;
-    if ((use_tc ? launch_tc_down(g, maps2, sms, s) : launch_gemm_down(additive, nrb, g, sms * ctas, s)) !=
-        cudaSuccess)
+    if ((tc_ok && launch_tc_down(g, maps2, sms, s) != cudaSuccess) ||
+        launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess)
         return EXL3_E_CUDA;
     prof_mark(4, s);
     return EXL3_OK;

@@ -489,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm
         n_items = a.n_items_host;
         split = a.split_host != 0;
     } else {
+        if (a.hdr[kHdrRegime] != 0)
+            return;                          // the prefill-regime kernels run this layer
         n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
         split = a.hdr[MODE == kModeGateUp ? kHdrSplit1 : kHdrSplit2] != 0;
         if (MODE == kModeDown && a.hdr[kHdrError] != 0) {

@@ -474,6 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
     int *kmax_slot = reinterpret_cast<int *>(smem + T::off_misc + 16);
 
+    if (a.hdr[kHdrRegime] != 1)
+        return;                              // the decode-regime kernels run this layer
     const int n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
     if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
         const size_t n = (size_t)a.M_tokens * a.out_f;
@@ -651,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
                 if (bg.rb != cur_rb) {
                     // slots of the old geometry overlap the new ones: drain the ring
-                    for (int bs = 0; ok && bs < kMaxBSlots; bs++)
-                        ok = reclaim(bs);
+                    for (int j = 0; ok && j < kMaxBSlots; j++)
+                        ok = reclaim(j);
                     bs = 0;
                     cur_rb = bg.rb;
                 }

@@ -17,6 +17,12 @@ namespace exl3 {
 struct RoutePackArgs {
     const void *ids;
     int R, E, capacity, rg_size, nw;
+    // fused layer regime model: rows per prefill-regime item (0: that regime
+    // is not allowed), rows per decode-regime row group of the plain forward
+    // and its cost in hundredths of a microsecond (8 rows: 1050, 16 rows:
+    // 1700).  A layer whose residual stages all have scale zero is the plain
+    // forward, so the model never depends on the stages.
+    int tc_rows, cost_rg, dec_unit_cost;
     int32_t *offsets, *packed, *tiles, *info;
     // fused-layer planning (plan != 0)
     int plan;

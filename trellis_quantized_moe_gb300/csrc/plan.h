@@ -31,6 +31,7 @@ enum HdrWord {
     kHdrSplit2 = 5,    // down / linear items split by chunk (0/1)
     kHdrNItems1 = 6,
     kHdrNItems2 = 7,
+    kHdrRegime = 8,    // fused layer: 0 = decode-regime kernels run, 1 = prefill (tcgen05) kernels
     kHdrWords = 64
 };
 

@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     if (tid == 0) {
         s_err = 0;
         a.info[kHdrError] = 0;
+        if (a.plan)
+            a.info[kHdrRegime] = 0;
     }
     __syncthreads();
 
@@ -121,11 +123,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     const int ntile_e = (tid < E) ? (cnt + a.capacity - 1) / a.capacity : 0;
     int ntiles;
     const int tile_off = block_exclusive_scan(ntile_e, s_warp, &ntiles);
+    // Regime choice (fused layer): both regimes decode a whole expert block
+    // once per work item, the decode regime per row group of rg_size rows, the
+    // prefill regime per item of up to tc_rows rows.  Measured cost per item
+    // (hidden 5120, inter 1536, K 3-4; other shapes scale both alike): decode
+    // regime 10.5 us (8-row groups) or 17 us (16-row groups), prefill regime
+    // 14.4 + 9.8 * rows / 256 us.  The regime with the smaller total wins; the
+    // choice depends only on the routing.
+    // (integer costs in hundredths, so the sums and the choice are exact)
+    // Residual stages with a nonzero scale on a routed expert need the decode
+    // regime (the prefill kernels carry no stages).
+    __shared__ long long s_cost[2];
+    __shared__ int s_tc, s_stage;
+    if (tid == 0) {
+        s_cost[0] = 0;
+        s_cost[1] = 0;
+        s_stage = 0;
+    }
+    __syncthreads();
+    if (tid < E && a.plan && a.tc_rows > 0 && cnt > 0) {
+        for (int s = 1; s < a.num_stages; s++)
+            for (int p = 0; p < 3; p++)
+                if (a.s_scale[((s - 1) * E + tid) * 3 + p] != 0.0f)
+                    s_stage = 1;
+        long long cd = 0, ct = 0;
+        for (int s = 0; s < ntile_e; s++) {
+            const int len = min(a.capacity, cnt - s * a.capacity);
+            cd += (long long)a.dec_unit_cost * ((len + a.cost_rg - 1) / a.cost_rg);
+            for (int r = 0; r < len; r += a.tc_rows)
+                ct += 1440 + 980 * min(a.tc_rows, len - r) / 256;
+        }
+        atomicAdd(reinterpret_cast<unsigned long long *>(&s_cost[0]), (unsigned long long)cd);
+        atomicAdd(reinterpret_cast<unsigned long long *>(&s_cost[1]), (unsigned long long)ct);
+    }
+    __syncthreads();
+    if (tid == 0)
+        s_tc = a.plan && a.tc_rows > 0 && !s_stage && s_cost[1] < s_cost[0];
+    __syncthreads();
+    const bool use_tc = s_tc != 0;
+    const int rg_size = use_tc ? a.tc_rows : a.rg_size;
     int nrg_e = 0;
     if (tid < E && a.plan) {
         for (int s = 0; s < ntile_e; s++) {
             int len = min(a.capacity, cnt - s * a.capacity);
-            nrg_e += (len + a.rg_size - 1) / a.rg_size;
+            nrg_e += (len + rg_size - 1) / rg_size;
         }
     }
     int n_rg;
@@ -181,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
             for (int s = 0; s < ntile_e; s++) {
                 const int start = off + s * a.capacity;
                 const int len = min(a.capacity, cnt - s * a.capacity);
-                for (int r = 0; r < len; r += a.rg_size)
-                    static_cast<int4 *>(a.rg)[k++] = make_int4(tid, start + r, min(a.rg_size, len - r), 0);
+                for (int r = 0; r < len; r += rg_size)
+                    static_cast<int4 *>(a.rg)[k++] = make_int4(tid, start + r, min(rg_size, len - r), 0);
             }
         }
     }
@@ -235,12 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
             a.info[kHdrNRg] = n_rg;
             const int pairs1 = n_rg * a.nb1, pairs2 = n_rg * a.nb2;
             const int lim = min(kSplitMaxPairs, 4 * a.num_sms);
-            const int split1 = a.nchunks1 > 1 && pairs1 <= min(lim, a.split_pairs1);
-            const int split2 = a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
+            // the prefill regime never splits the contraction
+            const int split1 = !use_tc && a.nchunks1 > 1 && pairs1 <= min(lim, a.split_pairs1);
+            const int split2 = !use_tc && a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
             a.info[kHdrSplit1] = split1;
             a.info[kHdrSplit2] = split2;
             a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
             a.info[kHdrNItems2] = split2 ? pairs2 * a.nchunks2 : pairs2;
+            a.info[kHdrRegime] = use_tc ? 1 : 0;
         }
     }
 }
