@@ -125,13 +125,52 @@ EXL3_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a 1 ms suspend-time hint: a waiting thread sleeps until the
+// phase completes (or the hint runs out) instead of re-polling, which leaves
+// the issue slots of its SM sub-partition to the warps that have work.
+EXL3_DEV bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+
+// x << N as an integer multiply: it issues on the FMA pipe, which the trellis
+// decode otherwise leaves mostly idle while shifts and logic ops share the ALU
+// pipe (both pipes take 16 lanes per cycle per SM sub-partition).
+template <int N>
+EXL3_DEV uint32_t shl_fma(uint32_t x)
+{
+    if constexpr (N == 0) {
+        return x;
+    } else {
+        uint32_t d;
+        asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(x), "n"(1u << N));
+        return d;
+    }
+}
+
+// The 16 bits of x starting N bits below its top (N <= 16): (x << N) >> 16,
+// the left shift on the FMA pipe and the right shift on the ALU pipe.
+template <int N>
+EXL3_DEV uint32_t bits16_from_top(uint32_t x)
+{
+    return shl_fma<N>(x) >> 16;
+}
+
 // Bounded wait: gives up after ~2^31 cycles and reports false.
 EXL3_DEV bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_try_wait_sleep(bar, parity))
         return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (clock64() - t0 > (1ll << 31))
             return false;
     }

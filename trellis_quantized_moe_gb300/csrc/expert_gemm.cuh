@@ -311,7 +311,7 @@ template <int K, int I>
 __device__ __forceinline__ uint32_t run_state(uint32_t X0, uint32_t X1)
 {
     if constexpr (I * K + 16 <= 32)
-        return (X0 >> (16 - I * K)) & 0xFFFFu;
+        return bits16_from_top<I * K>(X0);
     else
         return __funnelshift_l(X1, X0, I * K) >> 16;
 }

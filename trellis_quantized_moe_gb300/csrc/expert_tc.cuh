@@ -112,22 +112,6 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     return g;
 }
 
-// try_wait with a long suspend-time hint: a waiting thread sleeps until the
-// phase completes (or 1 ms passes) instead of re-polling, which leaves the
-// issue slots of its SM sub-partition to the decode warps.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
 // as soon as another thread has given up, and then reports false.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
@@ -277,6 +261,25 @@ struct ColumnWindow {
     }
 };
 
+// State i of the window (bits [iK, iK+16) of the normalised words X): one
+// FMA-pipe shift and one ALU shift when the state sits in one word.
+template <int K, int I>
+struct ColumnStates {
+    static __device__ __forceinline__ void run(const uint32_t *X, uint32_t *st)
+    {
+        constexpr int bit = I * K, q = bit >> 5, r = bit & 31;
+        if constexpr (r + 16 <= 32)
+            st[I] = bits16_from_top<r>(X[q]);
+        else
+            st[I] = __funnelshift_l(X[q + 1], X[q], r) >> 16;
+        ColumnStates<K, I + 1>::run(X, st);
+    }
+};
+template <int K>
+struct ColumnStates<K, 16> {
+    static __device__ __forceinline__ void run(const uint32_t *, uint32_t *) {}
+};
+
 // The 16 states of the window -> 16 fp16 weights in k order (8 half2 words):
 // mcg/3inst sum their two fp16 halves in fp16 (one rounding), mul1 gives the
 // exact integer byte sum - 510.
@@ -297,11 +300,11 @@ __device__ __forceinline__ void decode_column(const uint32_t *tile, const Column
         X[j] = __funnelshift_l(W[j + 1], W[j], cw.o);
     X[NX] = 0;
     uint32_t x[16];
+    uint32_t st[16];
+    ColumnStates<K, 0>::run(X, st);
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        const int bit = i * K, q = bit >> 5, r = bit & 31;
-        const uint32_t s = (r + 16 <= 32) ? ((X[q] >> ((16 - r) & 31)) & 0xFFFFu)
-                                          : (__funnelshift_l(X[q + 1], X[q], r) >> 16);
+        const uint32_t s = st[i];
         if (CB == EXL3_CB_MUL1)
             x[i] = __dp4a(s * A, 0x01010101u, 0x6400u);
         else
