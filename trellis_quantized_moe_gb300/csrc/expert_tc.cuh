@@ -12,8 +12,8 @@
 // contraction runs in one CTA (one persistent CTA per SM).  Roles:
 //   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 48 KB
 //               ring of stage slots sized by the layer's largest K (6 slots at
-//               K = 8, 12 at K = 4, 16 at K <= 3), mbarrier complete_tx, and
-//               prefetches later rows (also the next item's first ones) to L2;
+//               K = 8, 12 at K = 4, 16 at K <= 3), mbarrier complete_tx,
+//               running into the next item as slots free up;
 //   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
 //               256 columns = routes each); lane 0 issues tcgen05.mma
 //               (M=128, N=routes rounded up to 16, K=16) per stage and
@@ -49,7 +49,6 @@ constexpr int kStages = 3;        // decoded-weight (A) stages
 constexpr int kTwSlots = 16;      // trellis word slots (at most; sized by the layer's largest K)
 constexpr int kBRingBytes = 128 * 1024;   // activation (B) stages, sized per item
 constexpr int kMaxBSlots = 16;
-constexpr int kTwAhead = 16;      // trellis stages prefetched into L2 ahead
 constexpr int kTwRingBytes = 48 * 1024;
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
@@ -195,11 +194,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 template <int NREG>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NREG])
@@ -557,25 +551,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 return r;
             };
             auto row_of = [&](const Src &r, int p, int tk) { return r.tr[p] + (size_t)tk * ntn * (8 * r.K[p]); };
-            auto prefetch_stage = [&](const Src &r, int s) {
-                for (int p = 0; p < T::nproj; p++)
-                    for (int t = 0; t < T::T; t++)
-                        prefetch_l2_bulk(row_of(r, p, s * T::T + t), 256 * r.K[p]);
-            };
+            // (no separate L2 prefetch: measured slower, its requests compete
+            // with the ring's own copies)
             int item = blockIdx.x;
             Src cur = src_of(item);
-            for (int s = 0; s < kTwAhead && s < nst; s++)
-                prefetch_stage(cur, s);
             for (; item < n_items && !*abort; item += gridDim.x) {
                 const int next = item + (int)gridDim.x;
                 const Src nxt = next < n_items ? src_of(next) : cur;
                 for (int s = 0; s < nst; s++, rt.next()) {
-                    // rows kTwAhead stages ahead, running into the next item
-                    const int sp = s + kTwAhead;
-                    if (sp < nst)
-                        prefetch_stage(cur, sp);
-                    else if (next < n_items && sp - nst < nst)
-                        prefetch_stage(nxt, sp - nst);
                     const int slot = rt.slot;
                     if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
                         break;
