@@ -38,6 +38,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "rotate_block.cuh"
 
 namespace exl3 {
 namespace gemm {
@@ -527,14 +528,67 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm
     const int my_proj = (MODE == kModeGateUp) ? (warp >> 2) : 0;
     const bool root = (warp % T::group) == 0;
 
+    // fused input rotation: units per chunk = nproj x ROWS x 4 blocks, 8 per
+    // warp per pass; each lane's (projection, row) is fixed within an item,
+    // so its token and suh pointer are looked up once per item
+    constexpr int kRotUnits = T::nproj * ROWS * (kChunk / kHb);
+    constexpr int kRotPasses = MODE == kModeGateUp ? kRotUnits / (kWarps * 8) : 1;
+    static_assert(MODE != kModeGateUp || kRotPasses * kWarps * 8 == kRotUnits, "rotation units");
+    int rot_tok[kRotPasses];
+    const uint16_t *rot_suh[kRotPasses];
+
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         Item it;
         load_item<MODE, NRB>(a, item, split, it);
+        if (MODE == kModeGateUp && a.fuse_rot) {
+#pragma unroll
+            for (int q = 0; q < kRotPasses; q++) {
+                const int u = (q * kWarps + warp) * 8 + (lane >> 2);
+                const int r = (u / (kChunk / kHb)) % ROWS;
+                const int p = u / (ROWS * (kChunk / kHb));
+                rot_tok[q] = r < it.nrows ? a.packed[it.row0 + r] / a.topk : -1;
+                rot_suh[q] = reinterpret_cast<const uint16_t *>(a.t_suh[it.e * 3 + p]);
+            }
+        }
 
         for (int chunk = it.c_begin; chunk < it.c_end; chunk++) {
             // ---- activations of this chunk: [nproj][ROWS][512] fp16
             named_barrier(1, kThreads);
-            {
+            if (MODE == kModeGateUp && a.fuse_rot) {
+                // rotate x rows here: unit = (projection, row, 128-block of
+                // the chunk), four lanes per unit, the same arithmetic as the
+                // rotate kernel (identical fp16 bits)
+                const int c = lane & 3;
+#pragma unroll
+                for (int q = 0; q < kRotPasses; q++) {
+                    const int u = (q * kWarps + warp) * 8 + (lane >> 2);
+                    const int b = u % (kChunk / kHb);
+                    const int r = (u / (kChunk / kHb)) % ROWS;
+                    const int p = u / (ROWS * (kChunk / kHb));
+                    const int col = chunk * kChunk + b * kHb;
+                    const bool valid = rot_tok[q] >= 0 && col < a.in_f;
+                    float v[kRotFeat], sv[kRotFeat];
+                    if (valid) {
+                        const int tok = rot_tok[q];
+                        const uint16_t *suh = rot_suh[q];
+                        load_act32(a.x, (size_t)tok * a.in_f + col + kRotFeat * c, a.act_dtype, v);
+                        load_half32(suh, col + kRotFeat * c, sv);
+#pragma unroll
+                        for (int i = 0; i < kRotFeat; i++)
+                            v[i] *= sv[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kRotFeat; i++)
+                            v[i] = 0.0f;
+                    }
+                    uint4 o[4];
+                    rotate_block32(v, c, o);
+                    uint4 *dst = reinterpret_cast<uint4 *>(act_s + (p * ROWS + r) * kActLd + b * kHb + kRotFeat * c);
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        dst[k] = o[k];
+                }
+            } else {
                 const int c0 = chunk * kChunk;
                 const int nvec = T::nproj * ROWS * (kChunk / 8);
                 for (int v = tid; v < nvec; v += kThreads) {

@@ -24,6 +24,8 @@ struct RoutePackArgs {
     // forward, so the model never depends on the stages.
     int tc_rows, cost_rg, dec_unit_cost;
     int32_t *offsets, *packed, *tiles, *info;
+    int32_t *zero;                  // words to clear (per-call counters), or null
+    int nzero;
     // fused-layer planning (plan != 0)
     int plan;
     void *rg;                       // int4 [max_rg] = (expert, first row, rows, 0)
@@ -64,6 +66,10 @@ struct GemmArgs {
     int M, n_items_host, split_host;
     const uint16_t *act;            // fp16 rows (rotated activations)
     long act_row_stride;            // halves between rows
+    // gate/up of small decode-regime layers: rotate the raw activations x
+    // (act_dtype, [M][in_f]) while loading each chunk instead of reading act
+    const void *x;
+    int fuse_rot;
     // expert tables (fused layer)
     const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
     const int32_t *t_K, *t_cb;

@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
 
     for (int i = tid; i < nw * E; i += kThreads)
         hist[i] = 0;
+    for (int i = tid; i < a.nzero; i += kThreads)
+        a.zero[i] = 0;
     if (tid == 0) {
         s_err = 0;
         a.info[kHdrError] = 0;
