@@ -164,6 +164,12 @@ EXL3_DEV uint32_t bits16_from_top(uint32_t x)
     return shl_fma<N>(x) >> 16;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the stream
+// has completed and its writes are visible; allow the next kernel to start
+// launching.  Both are no-ops in a kernel launched without the attribute.
+EXL3_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+EXL3_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Bounded wait: gives up after ~2^31 cycles and reports false.
 EXL3_DEV bool mbar_wait(uint64_t *bar, uint32_t parity)
 {

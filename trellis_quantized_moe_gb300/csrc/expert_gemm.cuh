@@ -484,26 +484,31 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    // Programmatic dependent launch (decode-regime layers): gate/up and linear
+    // wait for their predecessor at once and let the next kernel launch; down
+    // first reads the plan (written by the route-pack kernel, complete before
+    // gate/up passed its wait) and starts streaming its trellis words, then
+    // waits for gate/up before touching its outputs.  Every CTA waits before
+    // it exits, so each kernel completes after its predecessor.
+    if (MODE != kModeDown) {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
     int n_items;
     bool split;
     if (MODE == kModeLinear) {
         n_items = a.n_items_host;
         split = a.split_host != 0;
     } else {
-        if (a.hdr[kHdrRegime] != 0)
+        if (a.hdr[kHdrRegime] != 0) {
+            grid_dep_wait();
             return;                          // the prefill-regime kernels run this layer
+        }
         n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
         split = a.hdr[MODE == kModeGateUp ? kHdrSplit1 : kHdrSplit2] != 0;
-        if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
-            // device-detected contract violation: zero-filled output
-            const size_t n = (size_t)a.M_tokens * a.out_f;
-            for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n;
-                 i += (size_t)gridDim.x * kThreads)
-                reinterpret_cast<uint16_t *>(a.out)[i] = 0;
-            return;
-        }
     }
-    if ((int)blockIdx.x >= n_items)
+    const bool work = (int)blockIdx.x < n_items;
+    if (MODE != kModeDown && !work)
         return;
 
     Ring ring;
@@ -512,17 +517,35 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm
     ring.ws = reinterpret_cast<WarpStream *>(smem + S::ws_off) + warp;
     ring.head = 0;
     ring.dead = false;
-    if (lane == 0) {
+    if (work) {
+        if (lane == 0) {
+            for (int s = 0; s < kSlots; s++)
+                mbar_init(&ring.bar[s], 1);
+            fence_mbar_init();
+            producer_init<MODE, NRB, ADD>(a, ring.ws->P, n_items, split);
+            ring.ws->issued = 0;
+            ring.ws->dead = 0;
+        }
+        __syncwarp();
         for (int s = 0; s < kSlots; s++)
-            mbar_init(&ring.bar[s], 1);
-        fence_mbar_init();
-        producer_init<MODE, NRB, ADD>(a, ring.ws->P, n_items, split);
-        ring.ws->issued = 0;
-        ring.ws->dead = 0;
+            ring_issue<MODE, NRB, ADD>(ring, a, warp);
     }
-    __syncwarp();
-    for (int s = 0; s < kSlots; s++)
-        ring_issue<MODE, NRB, ADD>(ring, a, warp);
+    if (MODE == kModeDown) {
+        grid_dep_wait();
+        if (a.hdr[kHdrError] != 0) {
+            // device-detected contract violation: zero-filled output (every
+            // CTA of the grid takes part)
+            const size_t n = (size_t)a.M_tokens * a.out_f;
+            for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n;
+                 i += (size_t)gridDim.x * kThreads)
+                reinterpret_cast<uint16_t *>(a.out)[i] = 0;
+            if (work)
+                ring_drain(ring);
+            return;
+        }
+        if (!work)
+            return;
+    }
 
     const int npass = ADD ? a.num_stages : 1;
     const int my_proj = (MODE == kModeGateUp) ? (warp >> 2) : 0;
@@ -777,8 +800,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(NRB, ADD)) k_expert_gemm
 template <int MODE, int NRB, bool ADD>
 cudaError_t launch_one(const GemmArgs &a, int grid, cudaStream_t s)
 {
-    k_expert_gemm<MODE, NRB, ADD><<<grid, kThreads, SmemPlan<MODE, NRB>::total, s>>>(a);
-    return cudaGetLastError();
+    if (!a.pdl) {
+        k_expert_gemm<MODE, NRB, ADD><<<grid, kThreads, SmemPlan<MODE, NRB>::total, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SmemPlan<MODE, NRB>::total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_expert_gemm<MODE, NRB, ADD>, a);
 }
 
 template <int MODE, int NRB, bool ADD>

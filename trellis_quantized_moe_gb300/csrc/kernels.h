@@ -70,6 +70,9 @@ struct GemmArgs {
     // (act_dtype, [M][in_f]) while loading each chunk instead of reading act
     const void *x;
     int fuse_rot;
+    // launch with programmatic dependent launch (decode-regime layers): the
+    // kernel waits for its predecessor itself, before reading its outputs
+    int pdl;
     // expert tables (fused layer)
     const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
     const int32_t *t_K, *t_cb;
