@@ -107,6 +107,31 @@ def test_linear_shapes(M, in_f, out_f, act):
     assert_close_linear(y[rows], ref, act, f"linear {M}x{in_f}x{out_f}")
 
 
+@pytest.mark.parametrize("M,K,cb,act", [(300, 3, CB_MCG, "bf16"), (600, 5, CB_3INST, "f16"),
+                                        (129, 2, CB_MUL1, "f16")])
+def test_linear_prompt_rows_tcgen05(M, K, cb, act):
+    # more than 128 rows: the tcgen05 kernel (items of 256 rows; 300 and 600
+    # leave ragged last tiles, 129 a one-row tile); sampled rows from every tile
+    lw = LinearWorkload(M=M, in_f=1024, out_f=640, K=K, cb=cb, act=act, seed=M + K)
+    y = to_f64(_linear_gpu(lw))
+    rows = np.unique(np.array([0, 1, 127, 128, 255, 256, M // 2, M - 2, M - 1]) % M)
+    ref = O.linear(act_to_f64(lw.x, act)[rows], lw.proj)
+    assert_close_linear(y[rows], ref, act, f"linear tcgen05 M={M} K={K} cb={cb}")
+
+
+def test_linear_prompt_rows_do_not_depend_on_row_count():
+    # above 128 rows every output column is computed by the same tcgen05
+    # contraction whatever the tile's row count
+    big = LinearWorkload(M=600, in_f=1024, out_f=512, K=4, cb=CB_MCG, act="bf16", seed=5)
+    dp = X.DeviceProjection(big.proj)
+    y_big = _linear_gpu(big, dp).view(torch.int16).cpu().numpy()
+    for M in (129, 300, 513):
+        small = LinearWorkload(M=M, in_f=1024, out_f=512, K=4, cb=CB_MCG, act="bf16", seed=5)
+        small.x = big.x[:M]
+        y = _linear_gpu(small, dp).view(torch.int16).cpu().numpy()
+        assert np.array_equal(y, y_big[:M]), M
+
+
 def test_linear_rows_are_byte_invariant_across_row_counts():
     big = LinearWorkload(M=128, in_f=5120, out_f=1536, K=3, cb=CB_MCG, act="bf16", seed=77)
     dp = X.DeviceProjection(big.proj)

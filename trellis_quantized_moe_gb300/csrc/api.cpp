@@ -12,6 +12,7 @@ using namespace exl3;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kLinearTcMinRows = 128;  // linear: more rows than this take the tcgen05 kernel
 constexpr int kPdlRoutes = 64;         // routes up to which gate/up -> down use programmatic dependent launch
 constexpr int kFuseRotRoutes = 32;     // routes up to which gate/up rotates its own inputs (measured: M=1 -7 us, M=8 +25 us)
 
@@ -439,6 +440,18 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
     g.part = reinterpret_cast<float *>(w + L.part);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = y;
+    if (M > kLinearTcMinRows) {
+        // prompt-sized inputs: the tcgen05 kernel, items of up to 256 rows x
+        // 128 outputs, the whole contraction per item (M <= 128 keeps the
+        // decode regime, so a row's bytes never depend on M there)
+        TcMaps maps;
+        if (!encode_act_maps(maps, ra.out, p->in_features, M, kTcKsDown))
+            return EXL3_E_CUDA;
+        g.split_host = 0;
+        g.n_items_host = ceil_div(M, tc_rows_per_item()) * L.nb;
+        const int grid = sms < g.n_items_host ? sms : g.n_items_host;
+        return launch_tc_linear(g, maps, grid, stream) == cudaSuccess ? EXL3_OK : EXL3_E_CUDA;
+    }
     int grid = sms * gemm_ctas_per_sm(2, false);
     if (grid > g.n_items_host)
         grid = g.n_items_host;

@@ -180,6 +180,26 @@ __device__ __forceinline__ void epi_down_combine_rows(const GemmArgs &a, int nbk
     }
 }
 
+// linear (one projection): the per-column factors, loaded once per block
+__device__ __forceinline__ void epi_linear_consts(const GemmArgs &a, int nbk, DownConsts &c)
+{
+    const int col = nbk * kHb + 4 * (threadIdx.x & 31);
+    load_half4(a.lin.svh, col, c.sv);
+    load_half4(a.lin.scale, col, c.sc);
+}
+
+__device__ __forceinline__ void epi_linear_row(const GemmArgs &a, const DownConsts &c, int nbk, int row,
+                                               float z[4])
+{
+    const int lane = threadIdx.x & 31;
+    const int col = nbk * kHb + 4 * lane;
+    warp_hadamard128(z);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        z[i] = z[i] * kInvSqrt128 * c.sv[i] * c.sc[i];
+    store_act4(a.out, (size_t)row * a.out_f + col, a.act_dtype, z);
+}
+
 // linear: y = Hb(z)*svh*scale, stored in the activation dtype.
 __device__ __forceinline__ void epi_linear_row(const GemmArgs &a, int nbk, int row, float z[4])
 {

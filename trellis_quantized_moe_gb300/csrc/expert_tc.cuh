@@ -367,12 +367,20 @@ __device__ __forceinline__ TwGeom tw_geom(int kmax)
     return g;
 }
 
+// Item = (row group, 128-output block).  Fused layer: row groups from the
+// route-pack plan (one expert's packed routes); linear: 256 token rows.
 template <int MODE>
 __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 {
     TcItem it;
     const int rgi = item / a.nb;
     it.nbk = item % a.nb;
+    if (MODE == kModeLinear) {
+        it.e = 0;
+        it.row0 = rgi * kNT;
+        it.nrows = min(kNT, a.M - it.row0);
+        return it;
+    }
     const int4 r = static_cast<const int4 *>(a.rg)[rgi];
     it.e = r.x;
     it.row0 = r.y;
@@ -382,6 +390,30 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 
 template <int MODE>
 __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? p : 2; }
+
+// Projection p of expert e: trellis words, width, codebook (linear: its one
+// projection).
+struct ProjRef {
+    const uint32_t *trellis;
+    int K, cb;
+};
+
+template <int MODE>
+__device__ __forceinline__ ProjRef proj_ref(const GemmArgs &a, int e, int p)
+{
+    ProjRef r;
+    if (MODE == kModeLinear) {
+        r.trellis = a.lin.trellis;
+        r.K = a.lin.K;
+        r.cb = a.lin.codebook;
+    } else {
+        const int i = e * 3 + proj_index<MODE>(p);
+        r.trellis = reinterpret_cast<const uint32_t *>(a.t_trellis[i]);
+        r.K = a.t_K[i];
+        r.cb = a.t_cb[i];
+    }
+    return r;
+}
 
 // All stages of one work item for one decode thread: trellis words -> decoded
 // A tile, one arrival per warp on the stage barrier.  K and the codebook are
@@ -471,9 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
     int *kmax_slot = reinterpret_cast<int *>(smem + T::off_misc + 16);
 
-    if (a.hdr[kHdrRegime] != 1)
+    if (MODE != kModeLinear && a.hdr[kHdrRegime] != 1)
         return;                              // the decode-regime kernels run this layer
-    const int n_items = a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
+    const int n_items = MODE == kModeLinear ? a.n_items_host
+                                            : a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
     if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
         const size_t n = (size_t)a.M_tokens * a.out_f;
         for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n; i += (size_t)gridDim.x * kThreads)
@@ -506,9 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     if (warp == 0) {
         // the largest K of this kernel's projections sizes the trellis slots
         int km = 1;
-        for (int e = lane; e < a.E; e += 32)
-            for (int p = 0; p < T::nproj; p++)
-                km = max(km, min(8, a.t_K[e * 3 + proj_index<MODE>(p)]));
+        if (MODE == kModeLinear)
+            km = max(1, min(8, a.lin.K));
+        else
+            for (int e = lane; e < a.E; e += 32)
+                for (int p = 0; p < T::nproj; p++)
+                    km = max(km, min(8, a.t_K[e * 3 + proj_index<MODE>(p)]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             km = max(km, __shfl_xor_sync(0xffffffffu, km, o));
@@ -543,9 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 Src r;
                 r.bytes = 0;
                 for (int p = 0; p < T::nproj; p++) {
-                    const int i = it.e * 3 + proj_index<MODE>(p);
-                    r.K[p] = a.t_K[i];
-                    r.tr[p] = reinterpret_cast<const uint32_t *>(a.t_trellis[i]) + (size_t)it.nbk * 8 * (8 * r.K[p]);
+                    const ProjRef pr = proj_ref<MODE>(a, it.e, p);
+                    r.K[p] = pr.K;
+                    r.tr[p] = pr.trellis + (size_t)it.nbk * 8 * (8 * r.K[p]);
                     r.bytes += T::T * 256 * r.K[p];
                 }
                 return r;
@@ -673,8 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         uint32_t nit = 0;
         for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
             const TcItem it = tc_item<MODE>(a, item);
-            const int pi = it.e * 3 + proj_index<MODE>(p);
-            const int K = a.t_K[pi], cb = a.t_cb[pi];
+            const ProjRef pr = proj_ref<MODE>(a, it.e, p);
+            const int K = pr.K, cb = pr.cb;
             bool ok;
             switch (K) {
                 case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
@@ -697,11 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             DownConsts cd;
             if (MODE == kModeGateUp)
                 epi_gateup_consts(a, it.e, it.nbk, cg);
+            else if (MODE == kModeLinear)
+                epi_linear_consts(a, it.nbk, cd);
             else
                 epi_down_consts(a, it.e, it.nbk, cd);
             float fac[2];
             for (int pp = 0; pp < T::nproj; pp++)
-                fac[pp] = (a.t_cb[it.e * 3 + proj_index<MODE>(pp)] == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+                fac[pp] = (proj_ref<MODE>(a, it.e, pp).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
             // the four warps of a lane quarter split the interval's columns
             const int jq = dw >> 2;
             for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
@@ -738,7 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
 #pragma unroll
                             for (int i = 0; i < 4; i++)
                                 z[i] = zs[rr * kZsLd + 4 * lane + i];
-                            epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
+                            if (MODE == kModeLinear)
+                                epi_linear_row(a, cd, it.nbk, it.row0 + r, z);
+                            else
+                                epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
                         }
                     }
                 }

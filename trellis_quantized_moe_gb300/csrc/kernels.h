@@ -117,6 +117,7 @@ struct TcMaps {
 };
 cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
+cudaError_t launch_tc_linear(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t tc_set_attributes();
 int tc_rows_per_item();
 cudaError_t gemm_gateup_set_attributes();

@@ -1,4 +1,4 @@
-// Prefill-regime (tcgen05 / TMEM) gate/up and down kernels (see expert_tc.cuh).
+// Prefill-regime (tcgen05 / TMEM) gate/up, down and linear kernels (see expert_tc.cuh).
 #include "expert_tc.cuh"
 
 namespace exl3 {
@@ -13,9 +13,16 @@ cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cuda
     return tc::launch_tc<kModeDown>(a, maps, grid, s);
 }
 
+cudaError_t launch_tc_linear(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s)
+{
+    return tc::launch_tc<kModeLinear>(a, maps, grid, s);
+}
+
 cudaError_t tc_set_attributes()
 {
     cudaError_t e = tc::set_attr_tc<kModeGateUp>();
+    if (e == cudaSuccess)
+        e = tc::set_attr_tc<kModeLinear>();
     return e != cudaSuccess ? e : tc::set_attr_tc<kModeDown>();
 }
 
