@@ -398,6 +398,23 @@ def run_ours(args):
     del pex, pws
     torch.cuda.empty_cache()
 
+    # ---------------- prompt-sized linear (one projection, no routing)
+    from workloads import CB_MCG, LinearWorkload
+    lw = LinearWorkload(M=4096, in_f=5120, out_f=1536, K=3, cb=CB_MCG, act="bf16", seed=41)
+    ldp = X.DeviceProjection(lw.proj)
+    lx = torch.from_numpy(lw.x.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+    ly = torch.empty((lw.M, 1536), dtype=torch.bfloat16, device=dev)
+    lws = torch.empty(X.exl3_linear_workspace_bytes(lw.M, 5120, 1536), dtype=torch.uint8, device=dev)
+    l_ms, _, _ = timed(lambda: X.exl3_linear(lx, ldp, ly, lws), max(3, min(10, args.steps // 5)), 2)
+    lt = float(np.mean(l_ms))
+    lflops = 2.0 * lw.M * 5120 * 1536
+    linear = {"workload": "EXL3 linear 5120 -> 1536, K=3 mcg, bf16, M=4096 rows",
+              "us": 1e3 * lt, "rows_per_s": lw.M / (lt * 1e-3),
+              "tflops_dense_equiv": lflops / (lt * 1e-3) / 1e12,
+              "frac_of_fp16_peak": lflops / (lt * 1e-3) / 1e12 / bf16_peak}
+    del ldp, lws
+    torch.cuda.empty_cache()
+
     if rank != 0:
         return
     cpu = cpu_baseline()
@@ -426,6 +443,7 @@ def run_ours(args):
                                   "peak_source": peak_src}},
         "sweep": sweep,
         "prefill_m3072": prefill,
+        "linear_m4096": linear,
         "e2e": {"value": world * 1 / (e_t * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
