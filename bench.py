@@ -448,7 +448,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "gpu_launches": 4 * args.steps,
+        # route pack, (rotate,) gate/up, down: layers of up to 32 routes rotate
+        # inside the gate/up kernel
+        "gpu_launches": (3 if 1 * spec.topk <= 32 else 4) * args.steps,
         "wall_s_timed_region": wall,
     }
     print(json.dumps(line))
