@@ -354,6 +354,27 @@ def run_ours(args):
                            "layer_frac_hbm": b / (tm * 1e-3) / 1e9 / hbm_peak,
                            "kernel_us": [1e3 * float(v) for v in m_kern.mean(axis=0)]}
 
+    # ---------------- the M=1 layer captured once in a CUDA graph and replayed
+    def graph_timing():
+        try:
+            g = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            cs.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(cs):
+                layer(1)()                       # warm-up outside the capture
+                cs.synchronize()
+                with torch.cuda.graph(g, stream=cs):
+                    layer(1)()
+            torch.cuda.synchronize()
+            g_ms, _, _ = timed(g.replay, args.steps, args.warmup)
+            t = _max_over_ranks(dist, float(np.mean(g_ms)))
+            return {"us": 1e3 * t, "tokens_per_s": world / (t * 1e-3)}
+        except Exception as exc:                 # reported, not fatal
+            return {"error": str(exc).splitlines()[0][:200]}
+
+    graph = graph_timing()
+    assert X.exl3_workspace_error(ws) == 0
+
     # ---------------- end to end through the C ABI with host buffers (M=1)
     x_d, ids_d, rw_d, out_d = inputs[1]
     x_h = x_d.cpu().pin_memory()
@@ -442,6 +463,7 @@ def run_ours(args):
                                   "frac": achieved / hbm_peak, "algorithmic_bytes": gu_bytes,
                                   "peak_source": peak_src}},
         "sweep": sweep,
+        "graph_replay_m1": graph,
         "prefill_m3072": prefill,
         "linear_m4096": linear,
         "e2e": {"value": world * 1 / (e_t * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,

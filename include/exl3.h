@@ -37,7 +37,10 @@
  *     pointer after it returns; every call only enqueues kernels on `stream`,
  *     so calls can be captured in a CUDA graph.  The first call on a device
  *     sets kernel attributes and reads device attributes; make it outside
- *     stream capture.
+ *     stream capture (inside one it returns EXL3_E_CUDA).  While `stream` is
+ *     capturing, the checks that pointers live on the stream's device are
+ *     skipped (those queries cannot run on a capturing stream); an eager
+ *     call with the same arguments performs them.
  *   - A negative return is a contract violation found on the host; nothing
  *     was written to device memory and nothing was launched.
  *   - Contracts that only the device can check (route ids in [0, E), each

@@ -207,6 +207,35 @@ def test_decode_layer_parity(M, tokens):
     assert_close(out[rows], oracle_rows(w, tokens=rows), f"config 1 M={M}")
 
 
+@pytest.mark.parametrize("cfg,M", [(1, 1), (1, 32), (0, 16)])
+def test_layer_replayed_from_a_cuda_graph_matches_eager(cfg, M):
+    # the forward allocates and synchronises nothing, so it can be captured;
+    # the replay (with the dependent launches of small layers inside the
+    # graph) writes the same bytes as the eager call
+    w = MoEWorkload(config(cfg, M=M))
+    s = w.spec
+    ex = _experts(cfg)
+    x, ids, rw = moe_inputs(w)
+    ws = torch.empty(X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter, s.capacity),
+                     dtype=torch.uint8, device="cuda")
+    eager = out_tensor(w)
+    X.exl3_moe_forward(x, ids, rw, ex, s.capacity, ws, eager)
+    torch.cuda.synchronize()
+    out = out_tensor(w)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g, stream=cs):
+            X.exl3_moe_forward(x, ids, rw, ex, s.capacity, ws, out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert X.exl3_workspace_error(ws) == 0
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
 def test_decode_layer_rows_byte_invariant_across_batch_sizes():
     ref = None
     for M in (1, 2, 8, 32, 128):

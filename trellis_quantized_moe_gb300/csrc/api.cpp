@@ -31,13 +31,27 @@ void prof_mark(int i, cudaStream_t s)
         cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[i]), s);
 }
 
+// True while the calling thread's call is being recorded into a CUDA graph:
+// the stream-device and pointer-residency queries are skipped then (they fail
+// on a capturing stream and would invalidate the capture); the eager calls
+// that must precede any capture run them.
+thread_local bool g_capturing = false;
+
 // Device of the stream (must be the current device); lazily sets kernel attributes.
 int setup_device(cudaStream_t s, int *dev_out, int *sms_out)
 {
     int cur = -1, dev = -1;
     if (cudaGetDevice(&cur) != cudaSuccess)
         return EXL3_E_CUDA;
-    if (cudaStreamGetDevice(s, &dev) != cudaSuccess) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return EXL3_E_DEVICE;
+    }
+    g_capturing = cs != cudaStreamCaptureStatusNone;
+    if (g_capturing) {
+        dev = cur;
+    } else if (cudaStreamGetDevice(s, &dev) != cudaSuccess) {
         cudaGetLastError();
         return EXL3_E_DEVICE;
     }
@@ -46,6 +60,8 @@ int setup_device(cudaStream_t s, int *dev_out, int *sms_out)
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState &d = g_dev[dev];
     if (!d.ready) {
+        if (g_capturing)
+            return EXL3_E_CUDA;              // the first call per device sets kernel attributes
         if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return EXL3_E_CUDA;
         if (route_pack_set_attributes() != cudaSuccess || gemm_gateup_set_attributes() != cudaSuccess ||
@@ -61,6 +77,8 @@ int setup_device(cudaStream_t s, int *dev_out, int *sms_out)
 
 bool on_device(const void *p, int dev)
 {
+    if (g_capturing)
+        return true;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();
