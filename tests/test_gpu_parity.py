@@ -322,6 +322,28 @@ def test_additive_layer_parity_and_zero_scale_identity():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("M", [24, 300])
+def test_three_residual_stages_of_mixed_widths(M):
+    # S = 4 (base + stages of K = 3, 1, 5, mcg, base rotations), some alpha
+    # exactly 0; above 128 tokens active stages keep the decode regime
+    from workloads import MoESpec
+    E = 8
+    spec = MoESpec("stages", 512, 256, E, 2, M, "f16", "i32", "f32", np.full(E, 4),
+                   np.array([CB_MCG, CB_3INST, CB_MUL1, CB_MCG] * 2), seed=90 + M,
+                   residual_K=[3, 1, 5], residual_zero_frac=0.3)
+    w = MoEWorkload(spec)
+    ex = X.DeviceExperts.from_workload(w)
+    st = _stages(w)
+    out = to_f64(run_layer(w, ex, stages=st))
+    assert LAST["regime"] == 0
+    assert_close_linear(out, oracle_rows(w), "f16", f"three stages M={M}")
+    zero = _stages(w)
+    zero.t_scale.zero_()
+    a = run_layer(w, ex, stages=zero).view(torch.int16).cpu().numpy()
+    b = run_layer(w, ex).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
 # --------------------------------------------------------------------------- contracts
 def test_host_contract_violation_writes_nothing():
     import ctypes
