@@ -46,10 +46,16 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def _src_hash():
+# Sources the decode-regime gate/up kernel is compiled from: its DRAM traffic
+# in profiles/traffic.json is valid while these are unchanged.
+GATE_UP_SOURCES = ("expert_gemm.cuh", "gemm_gateup.cu", "common.cuh", "epilogue.cuh",
+                   "rotate_block.cuh", "kernels.h", "plan.h")
+
+
+def _src_hash(files=GATE_UP_SOURCES):
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "trellis_quantized_moe_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in files:
+        with open(os.path.join(ROOT, "trellis_quantized_moe_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
