@@ -112,19 +112,6 @@ EXL3_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
                  : "memory");
 }
 
-EXL3_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // try_wait with a 1 ms suspend-time hint: a waiting thread sleeps until the
 // phase completes (or the hint runs out) instead of re-polling, which leaves
 // the issue slots of its SM sub-partition to the warps that have work.
@@ -192,13 +179,6 @@ EXL3_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar
         : "memory");
 }
 
-EXL3_DEV uint32_t lds_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
 EXL3_DEV void named_barrier(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -220,33 +200,6 @@ EXL3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// x >> 16 as the high word of x * 2^16 (runs on the FMA pipe, not the ALU pipe)
-EXL3_DEV uint32_t hi16_fma(uint32_t x)
-{
-    uint32_t d;
-    asm("mul.hi.u32 %0, %1, 65536;" : "=r"(d) : "r"(x));
-    return d;
-}
-
-// x << n for a compile-time n, as a funnel shift (ALU pipe)
-template <int N>
-EXL3_DEV uint32_t shl_alu(uint32_t x)
-{
-    if (N == 0)
-        return x;
-    uint32_t d;
-    asm("shf.l.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(0u), "r"(x), "n"(N));
-    return d;
-}
-
-EXL3_DEV uint32_t lop_mask_xor(uint32_t x)
-{
-    // (x & 0x8FFF8FFF) ^ 0x3B603B60 as one three-input logic op
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(x), "r"(0x8FFF8FFFu), "r"(0x3B603B60u));
     return d;
 }
 
