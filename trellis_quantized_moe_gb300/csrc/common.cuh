@@ -196,6 +196,32 @@ EXL3_DEV void mma_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// (x & mask) ^ flip as one LOP3 (truth table 0x6A).  A LOP3 takes at most
+// one immediate, and an immediate constant that the compiler re-materialises
+// inside an unrolled decode loop costs a second logic instruction per weight,
+// so both constants are register operands here.
+EXL3_DEV uint32_t and_xor(uint32_t x, uint32_t mask, uint32_t flip)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(x), "r"(mask), "r"(flip));
+    return d;
+}
+
+// The mask and exponent flip that the mcg and 3inst codebooks apply to both
+// 16-bit halves of the hashed state, as register values for a whole decode
+// loop.  `zero` must be 0 at run time but unknown to the compiler (the low
+// address bit of an int32 pointer argument), which stops it from folding the
+// constants back into immediates.
+struct HashConsts {
+    uint32_t mask, flip;
+};
+
+EXL3_DEV HashConsts hash_consts(const int32_t *aligned_ptr)
+{
+    const uint32_t zero = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(aligned_ptr) & 1u);
+    return {0x8FFF8FFFu ^ zero, 0x3B603B60u ^ zero};
+}
+
 EXL3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
     uint32_t d;

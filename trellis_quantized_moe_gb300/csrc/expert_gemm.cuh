@@ -45,8 +45,8 @@ namespace gemm {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 3;
-constexpr int kSlotBytes = 2048;           // 8 tiles x 32*K bytes, K <= 8
+constexpr int kSlots = 2;
+constexpr int kSlotBytes = 3072;           // whole tk rows of 8 tiles (32*K bytes each), K <= 8
 constexpr int kActLd = kChunk + 16;        // halves per activation row in smem
 constexpr int kZsLd = kHb + 4;             // floats per row of the z tile
 
@@ -345,6 +345,7 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
     constexpr uint32_t mul = Codebook<CB>::a, add = Codebook<CB>::b;
 
     constexpr int RPS = rows_per_slot(K);
+    const HashConsts hc = hash_consts(a.hdr);
     for (int tk_s = ps.tk0; tk_s < ps.tk1; tk_s += RPS) {
         const int nrows = min(RPS, ps.tk1 - tk_s);
         const uint32_t *seg = ring_wait(ring, a.hdr);
@@ -407,8 +408,8 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
                     uint32_t xA[4], xB[4];
 #pragma unroll
                     for (int i = 0; i < 4; i++) {
-                        xA[i] = ((sA[i] * mul + add) & 0x8FFF8FFFu) ^ 0x3B603B60u;
-                        xB[i] = ((sB[i] * mul + add) & 0x8FFF8FFFu) ^ 0x3B603B60u;
+                        xA[i] = and_xor(sA[i] * mul + add, hc.mask, hc.flip);
+                        xB[i] = and_xor(sB[i] * mul + add, hc.mask, hc.flip);
                     }
 #pragma unroll
                     for (int nb = 0; nb < NRB; nb++) {

@@ -279,7 +279,7 @@ struct ColumnStates<K, 16> {
 // exact integer byte sum - 510.
 template <int K, int CB>
 __device__ __forceinline__ void decode_column(const uint32_t *tile, const ColumnWindow<K> &cw,
-                                              uint32_t w[8])
+                                              const HashConsts &hc, uint32_t w[8])
 {
     constexpr int NX = ColumnWindow<K>::NX;
     constexpr uint32_t A = CB == EXL3_CB_MUL1 ? 0x83DCD12Du : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
@@ -302,7 +302,7 @@ __device__ __forceinline__ void decode_column(const uint32_t *tile, const Column
         if (CB == EXL3_CB_MUL1)
             x[i] = __dp4a(s * A, 0x01010101u, 0x6400u);
         else
-            x[i] = ((s * A + B) & 0x8FFF8FFFu) ^ 0x3B603B60u;
+            x[i] = and_xor(s * A + B, hc.mask, hc.flip);
     }
 #pragma unroll
     for (int i = 0; i < 8; i++) {
@@ -427,6 +427,7 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
     using T = Traits<MODE>;
     const int nst = a.in_f / T::KS;
     const ColumnWindow<K> cw(m & 15);
+    const HashConsts hc = hash_consts(a.hdr);
     const int tile_off = (p * T::T + t) * tg.row_bytes + (m >> 4) * 32 * K;          // bytes
     const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
     // two stages per pass (the stage count is even): twice the independent
@@ -442,10 +443,10 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
         uint32_t w0[8], w1[8];
         decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt.slot * tg.slot_bytes +
                                                                 tile_off),
-                             cw, w0);
+                             cw, hc, w0);
         decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt1.slot * tg.slot_bytes +
                                                                 tile_off),
-                             cw, w1);
+                             cw, hc, w1);
         warp_arrive(&B.twempty[rt.slot]);
         warp_arrive(&B.twempty[rt1.slot]);
         // an A slot is free once the MMA of its previous stage completed; the
