@@ -207,7 +207,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.tc_rows = tc_ok ? tc_rows_per_item() : 0;
     rp.cost_rg = 8 * nrb_plain;
     rp.dec_unit_cost = nrb_plain == 2 ? 1700 : 1050;
-    rp.nw = route_pack_hist_warps(E);
+    rp.nw = route_pack_hist_warps(E, rp.R);
     rp.offsets = reinterpret_cast<int32_t *>(w + L.offsets);
     rp.packed = reinterpret_cast<int32_t *>(w + L.packed);
     rp.tiles = reinterpret_cast<int32_t *>(w + L.tiles);
@@ -385,7 +385,7 @@ int exl3_route_pack(const void *ids, int ids_dtype, int M, int topk, int E, int 
     rp.E = E;
     rp.capacity = capacity;
     rp.rg_size = kRowGroup;
-    rp.nw = route_pack_hist_warps(E);
+    rp.nw = route_pack_hist_warps(E, rp.R);
     rp.offsets = offsets;
     rp.packed = packed;
     rp.tiles = tiles;

@@ -98,7 +98,7 @@ struct GemmArgs {
     int M_tokens;
 };
 
-int route_pack_hist_warps(int E);
+int route_pack_hist_warps(int E, int R);
 cudaError_t launch_route_pack(const RoutePackArgs &a, int ids_dtype, cudaStream_t s);
 cudaError_t route_pack_set_attributes();
 cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s);

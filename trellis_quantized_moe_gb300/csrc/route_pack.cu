@@ -290,9 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     }
 }
 
-int route_pack_hist_warps(int E)
+// Warps holding a histogram row: at most 32, at most 16384 counters of shared
+// memory, and no more than the 32-route steps there are (each warp walks the
+// per-expert rows when it sums counts and sets cursors, so idle rows cost time).
+int route_pack_hist_warps(int E, int R)
 {
     int nw = 16384 / (E > 0 ? E : 1);
+    const int steps = (R + 31) / 32;
+    nw = nw < steps ? nw : steps;
     return nw < 1 ? 1 : (nw > 32 ? 32 : nw);
 }
 
