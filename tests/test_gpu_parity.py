@@ -312,6 +312,7 @@ def test_additive_layer_parity_and_zero_scale_identity():
     ex = _experts(4)
     st = _stages(w)
     out = run_layer(w, ex, stages=st)
+    assert LAST["regime"] == 1            # ~14 routes per expert: the tcgen05 kernels
     rows = np.array([0, 255, 511])
     assert_close(to_f64(out)[rows], oracle_rows(w, tokens=rows), "config 4")
     # every stage at scale 0: bit-identical to the base-only forward
@@ -325,7 +326,9 @@ def test_additive_layer_parity_and_zero_scale_identity():
 @pytest.mark.parametrize("M", [24, 300])
 def test_three_residual_stages_of_mixed_widths(M):
     # S = 4 (base + stages of K = 3, 1, 5, mcg, base rotations), some alpha
-    # exactly 0; above 128 tokens active stages keep the decode regime
+    # exactly 0, bases of all three codebooks (a mul1 base scales its mcg
+    # residuals differently); above 128 tokens the tcgen05 kernels run the
+    # stages as extra passes over their accumulators
     from workloads import MoESpec
     E = 8
     spec = MoESpec("stages", 512, 256, E, 2, M, "f16", "i32", "f32", np.full(E, 4),
@@ -335,7 +338,7 @@ def test_three_residual_stages_of_mixed_widths(M):
     ex = X.DeviceExperts.from_workload(w)
     st = _stages(w)
     out = to_f64(run_layer(w, ex, stages=st))
-    assert LAST["regime"] == 0
+    assert LAST["regime"] == (0 if M <= 128 else 1)
     assert_close_linear(out, oracle_rows(w), "f16", f"three stages M={M}")
     zero = _stages(w)
     zero.t_scale.zero_()

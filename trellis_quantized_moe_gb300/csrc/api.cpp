@@ -182,12 +182,12 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     const int R = L.R;
     // Two regimes: decode (mma.sync; 16-row items at 1 CTA/SM when experts
     // carry more than 8 routes on average, else 8 rows; residual stages: 8
-    // rows) and prefill (tcgen05, up to 256 routes per item, no stages).  With
-    // more than 128 tokens both kernel pairs are launched and the route-pack
-    // kernel picks one from the per-expert route counts (the other pair
-    // returns at once); stages with a nonzero scale force the decode regime.
-    // M <= 128 always takes the decode regime, so a row's bytes never depend
-    // on M there.
+    // rows) and prefill (tcgen05, up to 256 routes per item; residual stages
+    // as extra passes over the same accumulators).  With more than 128 tokens
+    // both kernel pairs are launched and the route-pack kernel picks one from
+    // the per-expert route counts (the other pair returns at once).  M <= 128
+    // always takes the decode regime, so a row's bytes never depend on M
+    // there.
     const int active = E < R ? E : R;
     const bool tc_ok = M > 128;
     const int nrb_plain = R > 8 * active ? 2 : 1;

@@ -86,7 +86,8 @@ EXL3_DEV void warp_hadamard128(float v[4])
 }
 
 constexpr float kInvSqrt128 = 0.08838834764831845f;
-constexpr float kInvSqrtMul1 = 0.006765899173961108f;   // 1 / sqrt(21845)
+constexpr float kInvSqrtMul1 = 0.006765875086793228f;   // 1 / sqrt(21845)
+constexpr float kSqrtMul1 = 147.80054127099805f;        // sqrt(21845)
 
 // ---------------------------------------------------------------- mbarrier / bulk copy
 EXL3_DEV uint32_t smem_addr(const void *p)

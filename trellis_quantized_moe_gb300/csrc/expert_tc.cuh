@@ -415,17 +415,74 @@ __device__ __forceinline__ ProjRef proj_ref(const GemmArgs &a, int e, int p)
     return r;
 }
 
-// All stages of one work item for one decode thread: trellis words -> decoded
-// A tile, one arrival per warp on the stage barrier.  K and the codebook are
-// compile-time.
-template <int MODE, int K, int CB>
+// Residual stages ("MoE: Add fused additive EXL3 kernels", exllamav3 #284,
+// "Summary"): pass 0 of an item is the base weights, pass s = 1..num_stages-1
+// residual stage s, included when some projection of the item has a nonzero
+// scale there.  Every role walks the same passes, stage by stage.
+template <int MODE>
+__device__ __forceinline__ int tc_num_passes(const GemmArgs &a)
+{
+    return MODE == kModeLinear ? 1 : a.num_stages;
+}
+
+// Scale of projection p in pass s (1 for the base; 0 = stage skipped).
+template <int MODE>
+__device__ __forceinline__ float pass_alpha(const GemmArgs &a, int e, int p, int s)
+{
+    if (MODE == kModeLinear || s == 0)
+        return 1.0f;
+    return a.s_scale[((s - 1) * a.E + e) * 3 + proj_index<MODE>(p)];
+}
+
+template <int MODE>
+__device__ __forceinline__ bool pass_active(const GemmArgs &a, int e, int s)
+{
+    if (s == 0)
+        return true;
+    for (int p = 0; p < Traits<MODE>::nproj; p++)
+        if (pass_alpha<MODE>(a, e, p, s) != 0.0f)
+            return true;
+    return false;
+}
+
+// Trellis words, width and codebook of projection p in pass s (residuals are
+// mcg); only read where the pass's scale is nonzero.
+template <int MODE>
+__device__ __forceinline__ ProjRef pass_ref(const GemmArgs &a, int e, int p, int s)
+{
+    if (s == 0)
+        return proj_ref<MODE>(a, e, p);
+    const int j = ((s - 1) * a.E + e) * 3 + proj_index<MODE>(p);
+    ProjRef r;
+    r.trellis = reinterpret_cast<const uint32_t *>(a.s_trellis[j]);
+    r.K = a.s_K[j];
+    r.cb = EXL3_CB_MCG;
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 b)
+{
+    __half2 x = *reinterpret_cast<__half2 *>(&a);
+    x = __hmul2(x, b);
+    return *reinterpret_cast<uint32_t *>(&x);
+}
+
+// All stages of one pass of a work item for one decode thread: trellis words
+// -> decoded A tile (times the pass's scale), one arrival per warp on the
+// stage barrier.  K and the codebook are compile-time.  A thread whose
+// projection sits this pass out (scale 0) keeps the barrier rhythm without
+// touching the trellis slot or its A tile.  RES: a residual pass (the base
+// pass compiles without the scale and the skip).
+template <int MODE, int K, int CB, bool RES>
 __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
                                           volatile int *abort, const TcItem &it,
                                           RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
-                                          int p, int t, int m)
+                                          int p, int t, int m, bool active, float alpha)
 {
     using T = Traits<MODE>;
     const int nst = a.in_f / T::KS;
+    const bool act = !RES || active;
+    const __half2 alpha2 = __float2half2_rn(alpha);
     const ColumnWindow<K> cw(m & 15);
     const HashConsts hc = hash_consts(a.hdr);
     const int tile_off = (p * T::T + t) * tg.row_bytes + (m >> 4) * 32 * K;          // bytes
@@ -441,12 +498,21 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
             !wait_bar(&B.twfull[rt1.slot], rt1.phase, abort, a.hdr))
             return false;
         uint32_t w0[8], w1[8];
-        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt.slot * tg.slot_bytes +
-                                                                tile_off),
-                             cw, hc, w0);
-        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt1.slot * tg.slot_bytes +
-                                                                tile_off),
-                             cw, hc, w1);
+        if (act) {
+            decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt.slot * tg.slot_bytes +
+                                                                    tile_off),
+                                 cw, hc, w0);
+            decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt1.slot * tg.slot_bytes +
+                                                                    tile_off),
+                                 cw, hc, w1);
+            if (RES) {
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    w0[i] = hmul2_u32(w0[i], alpha2);
+                    w1[i] = hmul2_u32(w1[i], alpha2);
+                }
+            }
+        }
         warp_arrive(&B.twempty[rt.slot]);
         warp_arrive(&B.twempty[rt1.slot]);
         // an A slot is free once the MMA of its previous stage completed; the
@@ -456,10 +522,12 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
             return false;
         uint8_t *abuf0 = smem + T::off_a + ra.slot * T::nproj * T::a_bytes + a_off;
         uint8_t *abuf1 = smem + T::off_a + ra1.slot * T::nproj * T::a_bytes + a_off;
-        *reinterpret_cast<uint4 *>(abuf0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        *reinterpret_cast<uint4 *>(abuf0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-        *reinterpret_cast<uint4 *>(abuf1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        *reinterpret_cast<uint4 *>(abuf1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+        if (act) {
+            *reinterpret_cast<uint4 *>(abuf0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+            *reinterpret_cast<uint4 *>(abuf0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+            *reinterpret_cast<uint4 *>(abuf1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            *reinterpret_cast<uint4 *>(abuf1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         warp_arrive(&B.full[ra.slot]);
         warp_arrive(&B.full[ra1.slot]);
@@ -478,10 +546,67 @@ __device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t 
                                              int p, int t, int m)
 {
     if (cb == EXL3_CB_MUL1)
-        return tc_stages<MODE, K, EXL3_CB_MUL1>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_MUL1, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
     if (cb == EXL3_CB_3INST)
-        return tc_stages<MODE, K, EXL3_CB_3INST>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
-    return tc_stages<MODE, K, EXL3_CB_MCG>(a, smem, B, abort, it, ra, rt, tg, p, t, m);
+        return tc_stages<MODE, K, EXL3_CB_3INST, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
+    return tc_stages<MODE, K, EXL3_CB_MCG, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
+}
+
+// One decode thread's share of one work item: the base pass, then each
+// residual pass of the item.  A mul1 base is scaled by 1/sqrt(21845) in the
+// epilogue while the (mcg) residuals are not, so their scale carries
+// sqrt(21845) for such a projection.
+template <int MODE>
+__device__ __forceinline__ bool tc_item_decode(const GemmArgs &a, uint8_t *smem, const Bars &B,
+                                               volatile int *abort, const TcItem &it,
+                                               RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
+                                               int p, int t, int m)
+{
+    const ProjRef base = proj_ref<MODE>(a, it.e, p);
+    bool ok;
+    switch (base.K) {
+        case 1: ok = tc_stages_cb<MODE, 1>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 2: ok = tc_stages_cb<MODE, 2>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 3: ok = tc_stages_cb<MODE, 3>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 4: ok = tc_stages_cb<MODE, 4>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 5: ok = tc_stages_cb<MODE, 5>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 6: ok = tc_stages_cb<MODE, 6>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 7: ok = tc_stages_cb<MODE, 7>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        default: ok = tc_stages_cb<MODE, 8>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+    }
+    if (!ok || *abort)
+        return false;
+    const int npass = tc_num_passes<MODE>(a);
+    for (int s = 1; s < npass; s++) {
+        if (!pass_active<MODE>(a, it.e, s))
+            continue;
+        const float al = pass_alpha<MODE>(a, it.e, p, s);
+        const bool active = al != 0.0f;
+        const int K = active ? pass_ref<MODE>(a, it.e, p, s).K : 1;
+        const float alpha = base.cb == EXL3_CB_MUL1 ? al * kSqrtMul1 : al;
+#define EXL3_RES_CASE(KK)                                                                        \
+    case KK:                                                                                     \
+        ok = tc_stages<MODE, KK, EXL3_CB_MCG, true>(a, smem, B, abort, it, ra, rt, tg, p, t, m,  \
+                                                    active, alpha);                              \
+        break;
+        switch (K) {
+            EXL3_RES_CASE(1)
+            EXL3_RES_CASE(2)
+            EXL3_RES_CASE(3)
+            EXL3_RES_CASE(4)
+            EXL3_RES_CASE(5)
+            EXL3_RES_CASE(6)
+            EXL3_RES_CASE(7)
+            default:
+                ok = tc_stages<MODE, 8, EXL3_CB_MCG, true>(a, smem, B, abort, it, ra, rt, tg, p, t, m,
+                                                           active, alpha);
+                break;
+        }
+#undef EXL3_RES_CASE
+        if (!ok || *abort)
+            return false;
+    }
+    return true;
 }
 
 template <int MODE>
@@ -544,8 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             km = max(1, min(8, a.lin.K));
         else
             for (int e = lane; e < a.E; e += 32)
-                for (int p = 0; p < T::nproj; p++)
+                for (int p = 0; p < T::nproj; p++) {
                     km = max(km, min(8, a.t_K[e * 3 + proj_index<MODE>(p)]));
+                    for (int st = 1; st < tc_num_passes<MODE>(a); st++)
+                        if (pass_alpha<MODE>(a, e, p, st) != 0.0f)
+                            km = max(km, min(8, a.s_K[((st - 1) * a.E + e) * 3 + proj_index<MODE>(p)]));
+                }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             km = max(km, __shfl_xor_sync(0xffffffffu, km, o));
@@ -568,19 +697,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         if (lane == 0) {
             RingPosN rt;
             rt.n = tg.nslots;
-            // trellis rows of one item: first row of each projection's 128-output
-            // block, K per projection, bytes per stage
+            // trellis rows of one pass of an item: first row of each projection's
+            // 128-output block, K per projection, bytes per stage (projections
+            // with scale 0 in the pass stream nothing)
             struct Src {
                 const uint32_t *tr[2];
                 int K[2];
+                bool on[2];
                 uint32_t bytes;
             };
-            auto src_of = [&](int item) {
-                const TcItem it = tc_item<MODE>(a, item);
+            auto src_of = [&](const TcItem &it, int ps) {
                 Src r;
                 r.bytes = 0;
                 for (int p = 0; p < T::nproj; p++) {
-                    const ProjRef pr = proj_ref<MODE>(a, it.e, p);
+                    r.on[p] = pass_alpha<MODE>(a, it.e, p, ps) != 0.0f;
+                    r.K[p] = 1;
+                    r.tr[p] = nullptr;
+                    if (!r.on[p])
+                        continue;
+                    const ProjRef pr = pass_ref<MODE>(a, it.e, p, ps);
                     r.K[p] = pr.K;
                     r.tr[p] = pr.trellis + (size_t)it.nbk * 8 * (8 * r.K[p]);
                     r.bytes += T::T * 256 * r.K[p];
@@ -590,23 +725,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             auto row_of = [&](const Src &r, int p, int tk) { return r.tr[p] + (size_t)tk * ntn * (8 * r.K[p]); };
             // (no separate L2 prefetch: measured slower, its requests compete
             // with the ring's own copies)
+            const int npass = tc_num_passes<MODE>(a);
             int item = blockIdx.x;
-            Src cur = src_of(item);
+            TcItem cit = tc_item<MODE>(a, item);
+            Src cur = src_of(cit, 0);
             for (; item < n_items && !*abort; item += gridDim.x) {
+                // the next item's base rows are looked up while this one streams
                 const int next = item + (int)gridDim.x;
-                const Src nxt = next < n_items ? src_of(next) : cur;
-                for (int s = 0; s < nst; s++, rt.next()) {
-                    const int slot = rt.slot;
-                    if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
-                        break;
-                    uint8_t *dst = smem + T::off_tw + slot * tg.slot_bytes;
-                    mbar_arrive_expect_tx(&B.twfull[slot], cur.bytes);
-                    for (int p = 0; p < T::nproj; p++)
-                        for (int t = 0; t < T::T; t++)
-                            bulk_g2s(dst + (p * T::T + t) * tg.row_bytes, row_of(cur, p, s * T::T + t),
-                                     256 * cur.K[p], &B.twfull[slot]);
+                const TcItem nit = next < n_items ? tc_item<MODE>(a, next) : cit;
+                const Src nxt = next < n_items ? src_of(nit, 0) : cur;
+                for (int ps = 0; ps < npass && !*abort; ps++) {
+                    if (ps > 0 && !pass_active<MODE>(a, cit.e, ps))
+                        continue;
+                    const Src sp = ps == 0 ? cur : src_of(cit, ps);
+                    for (int s = 0; s < nst; s++, rt.next()) {
+                        const int slot = rt.slot;
+                        if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
+                            break;
+                        uint8_t *dst = smem + T::off_tw + slot * tg.slot_bytes;
+                        mbar_arrive_expect_tx(&B.twfull[slot], sp.bytes);
+                        for (int p = 0; p < T::nproj; p++)
+                            if (sp.on[p])
+                                for (int t = 0; t < T::T; t++)
+                                    bulk_g2s(dst + (p * T::T + t) * tg.row_bytes, row_of(sp, p, s * T::T + t),
+                                             256 * sp.K[p], &B.twfull[slot]);
+                    }
                 }
                 cur = nxt;
+                cit = nit;
             }
         }
     } else if (warp == 1) {
@@ -632,26 +778,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
                     break;
                 fence_after();
-                for (int s = 0; s < nst; s++, ra.next()) {
-                    const int slot = ra.slot;
-                    if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
-                        !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
-                        break;
-                    bphase ^= 1u << bs;
-                    fence_after();
-                    const uint64_t ad = adesc0 + (uint32_t)(slot * (T::nproj * T::a_bytes >> 4));
-                    const uint64_t bd = bdesc0 + (uint32_t)(bs * bstage16);
+                // pass 0 (base, every projection) opens each accumulator; the
+                // residual passes add to it
+                for (int ps = 0; ps < tc_num_passes<MODE>(a) && !*abort; ps++) {
+                    if (ps > 0 && !pass_active<MODE>(a, it.e, ps))
+                        continue;
+                    bool on[T::nproj];
 #pragma unroll
                     for (int p = 0; p < T::nproj; p++)
+                        on[p] = pass_alpha<MODE>(a, it.e, p, ps) != 0.0f;
+                    for (int s = 0; s < nst; s++, ra.next()) {
+                        const int slot = ra.slot;
+                        if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
+                            !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
+                            break;
+                        bphase ^= 1u << bs;
+                        fence_after();
+                        const uint64_t ad = adesc0 + (uint32_t)(slot * (T::nproj * T::a_bytes >> 4));
+                        const uint64_t bd = bdesc0 + (uint32_t)(bs * bstage16);
 #pragma unroll
-                        for (int ks = 0; ks < T::KS / 16; ks++)
-                            mma_f16(tmem + p * kNT, ad + (uint32_t)(p * (T::a_bytes >> 4) + ks * 16),
-                                    bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
-                                    (s > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(&B.empty[slot]);
-                    mma_commit(&B.bempty[bs]);
-                    if (++bs == bg.nslots)
-                        bs = 0;
+                        for (int p = 0; p < T::nproj; p++) {
+                            if (!on[p])
+                                continue;
+#pragma unroll
+                            for (int ks = 0; ks < T::KS / 16; ks++)
+                                mma_f16(tmem + p * kNT, ad + (uint32_t)(p * (T::a_bytes >> 4) + ks * 16),
+                                        bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
+                                        (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&B.empty[slot]);
+                        mma_commit(&B.bempty[bs]);
+                        if (++bs == bg.nslots)
+                            bs = 0;
+                    }
                 }
                 mma_commit(B.accfull);
             }
@@ -682,15 +841,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                     cur_rb = bg.rb;
                 }
                 const CUtensorMap *map = &maps.act[bg.map];
-                for (int s = 0; ok && s < nst; s++, bs = (bs + 1 == bg.nslots) ? 0 : bs + 1) {
-                    if (!(ok = reclaim(bs)))
-                        break;
-                    pend |= 1u << bs;
-                    uint8_t *dst = smem + T::off_b + bs * bg.stage_bytes;
-                    mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
-                    for (int p = 0; p < T::nproj; p++)
-                        tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
-                                    &B.bfull[bs]);
+                // the same activation tiles again for every residual pass
+                for (int ps = 0; ok && ps < tc_num_passes<MODE>(a); ps++) {
+                    if (ps > 0 && !pass_active<MODE>(a, it.e, ps))
+                        continue;
+                    for (int s = 0; ok && s < nst; s++, bs = (bs + 1 == bg.nslots) ? 0 : bs + 1) {
+                        if (!(ok = reclaim(bs)))
+                            break;
+                        pend |= 1u << bs;
+                        uint8_t *dst = smem + T::off_b + bs * bg.stage_bytes;
+                        mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
+                        for (int p = 0; p < T::nproj; p++)
+                            tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
+                                        &B.bfull[bs]);
+                    }
                 }
             }
             // every load this thread issued is consumed by an MMA before the
@@ -710,20 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         uint32_t nit = 0;
         for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
             const TcItem it = tc_item<MODE>(a, item);
-            const ProjRef pr = proj_ref<MODE>(a, it.e, p);
-            const int K = pr.K, cb = pr.cb;
-            bool ok;
-            switch (K) {
-                case 1: ok = tc_stages_cb<MODE, 1>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 2: ok = tc_stages_cb<MODE, 2>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 3: ok = tc_stages_cb<MODE, 3>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 4: ok = tc_stages_cb<MODE, 4>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 5: ok = tc_stages_cb<MODE, 5>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 6: ok = tc_stages_cb<MODE, 6>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                case 7: ok = tc_stages_cb<MODE, 7>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-                default: ok = tc_stages_cb<MODE, 8>(cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-            }
-            if (!ok || *abort)
+            if (!tc_item_decode<MODE>(a, smem, B, abort, it, ra, rt, tg, p, t, m) || *abort)
                 break;
             // ---- epilogue: TMEM -> shared (32 routes at a time) -> per-row epilogue
             if (!wait_bar(B.accfull, nit & 1, abort, a.hdr))

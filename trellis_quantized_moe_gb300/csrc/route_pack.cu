@@ -133,21 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     // 14.4 + 9.8 * rows / 256 us.  The regime with the smaller total wins; the
     // choice depends only on the routing.
     // (integer costs in hundredths, so the sums and the choice are exact)
-    // Residual stages with a nonzero scale on a routed expert need the decode
-    // regime (the prefill kernels carry no stages).
+    // Residual stages add the same decode work to both regimes and are left
+    // out, so a call whose stage scales are all 0 chooses as the plain
+    // forward does.
     __shared__ long long s_cost[2];
-    __shared__ int s_tc, s_stage;
+    __shared__ int s_tc;
     if (tid == 0) {
         s_cost[0] = 0;
         s_cost[1] = 0;
-        s_stage = 0;
     }
     __syncthreads();
     if (tid < E && a.plan && a.tc_rows > 0 && cnt > 0) {
-        for (int s = 1; s < a.num_stages; s++)
-            for (int p = 0; p < 3; p++)
-                if (a.s_scale[((s - 1) * E + tid) * 3 + p] != 0.0f)
-                    s_stage = 1;
         long long cd = 0, ct = 0;
         for (int s = 0; s < ntile_e; s++) {
             const int len = min(a.capacity, cnt - s * a.capacity);
@@ -160,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     }
     __syncthreads();
     if (tid == 0)
-        s_tc = a.plan && a.tc_rows > 0 && !s_stage && s_cost[1] < s_cost[0];
+        s_tc = a.plan && a.tc_rows > 0 && s_cost[1] < s_cost[0];
     __syncthreads();
     const bool use_tc = s_tc != 0;
     const int rg_size = use_tc ? a.tc_rows : a.rg_size;
