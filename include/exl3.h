@@ -190,10 +190,13 @@ int exl3_moe_forward(const void *x, int act_dtype, int M, int hidden, int inter,
 
 /* exl3_moe_forward plus additive residual stages (exllamav3 #284 "Summary":
  * exl3_moe_additive_fused).  For every projection the weights become
- * W_base + sum_s alpha_{s,e,p} W_{s,e,p}; each stage's contribution is scaled
- * by alpha in fp32 and added to an fp32 accumulator.  Entries with alpha == 0
- * read no bytes and run no MMA, so all-zero stages reproduce exl3_moe_forward
- * bit for bit.  stages: host struct holding device tables. */
+ * W_base + sum_s alpha_{s,e,p} W_{s,e,p}, accumulated in fp32: up to 128
+ * tokens each stage's partial sum is scaled by alpha in fp32 and added to the
+ * accumulator; above 128 tokens, when the tensor-core kernels run the layer,
+ * a stage is one more pass over the same fp32 accumulators with its decoded
+ * fp16 weights multiplied by alpha.  Entries with alpha == 0 read no bytes and
+ * run no MMA, so all-zero stages reproduce exl3_moe_forward bit for bit.
+ * stages: host struct holding device tables. */
 int exl3_moe_additive(const void *x, int act_dtype, int M, int hidden, int inter, int E,
                       int topk, const void *ids, int ids_dtype, const void *rw, int rw_dtype,
                       const exl3_experts *experts, const exl3_stages *stages, int capacity,

@@ -28,6 +28,9 @@
 //               with the decode-regime kernel;
 //   warp 18     lane 0 loads the activation (B) tiles with 2D TMA into a byte
 //               ring that runs as far ahead of the MMAs as it has room.
+// Additive layers: each residual stage with a nonzero scale on some
+// projection of the item is one more pass of stages that every role walks
+// in the same order, accumulating into the same TMEM columns.
 // A layout (K-major, no swizzle): element (r, k) of a stage tile sits at
 // (r/8)*SBO + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes, SBO = (KS/8)*128.
 // B layout (K-major, swizzled; one 2D TMA box {KS inputs, RB rows} per
