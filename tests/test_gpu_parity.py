@@ -393,3 +393,36 @@ def test_device_detected_bad_route_zero_fills_output():
     torch.cuda.synchronize()
     assert X.exl3_workspace_error(ws) & X.binding.DERR_ROUTE_ID
     assert torch.all(out == 0)
+
+
+def test_empty_batch_is_a_no_op():
+    # M = 0 (valid pointers, nothing to compute): every entry point returns OK
+    # and writes neither the output nor the workspace
+    import ctypes
+    w = MoEWorkload(config(0))
+    s = w.spec
+    x, ids, rw = moe_inputs(w)
+    ex = _experts(0)
+    st = ex.struct()
+    out = torch.full((s.M, s.hidden), 3.0, dtype=torch.float16, device="cuda")
+    nbytes = X.exl3_moe_workspace_bytes(16, s.topk, s.E, s.hidden, s.inter, s.capacity)
+    ws = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    lib = X.binding.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.exl3_moe_forward(x.data_ptr(), 0, 0, s.hidden, s.inter, s.E, s.topk, ids.data_ptr(),
+                              3, rw.data_ptr(), 0, ctypes.byref(st), s.capacity, ws.data_ptr(),
+                              nbytes, out.data_ptr(), stream)
+    assert rc == 0
+    lw = LinearWorkload(M=4, in_f=256, out_f=128, K=3, cb=CB_MCG, act="f16", seed=5)
+    dp = X.DeviceProjection(lw.proj)
+    ps = dp.struct()
+    xl = to_device(lw.x, lw.act)
+    y = torch.full((4, 128), 3.0, dtype=torch.float16, device="cuda")
+    lws = torch.full((X.exl3_linear_workspace_bytes(4, 256, 128),), 0x5A, dtype=torch.uint8,
+                     device="cuda")
+    rc = lib.exl3_linear(xl.data_ptr(), 0, 0, ctypes.byref(ps), y.data_ptr(), lws.data_ptr(),
+                         lws.numel(), stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0) and torch.all(ws == 0x5A)
+    assert torch.all(y == 3.0) and torch.all(lws == 0x5A)
