@@ -255,6 +255,22 @@ def _small_layer(M, act, seed, E=8, topk=2):
     return MoEWorkload(spec)
 
 
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_small_layer_rows_byte_invariant_across_batch_sizes(act):
+    # every width 1..8 and all three codebooks: a token's row at 16 tokens
+    # (32 routes: inputs rotated inside the gate/up kernel, chunks split over
+    # CTAs, 8-row items) equals its row at 40 tokens (80 routes: the rotate
+    # kernel, 16-row items) byte for byte, and both are within tolerance
+    small = _small_layer(16, act, 123)
+    large = _small_layer(40, act, 123)
+    ex = X.DeviceExperts.from_workload(large)
+    a = run_layer(small, ex).view(torch.int16).cpu().numpy()
+    b = run_layer(large, ex).view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b[:16])
+    got = to_f64(run_layer(small, ex))
+    assert_close(got, oracle_rows(small), f"16 tokens {act}")
+
+
 @pytest.mark.parametrize("M,act", [(512, "f16"), (1100, "bf16")])
 def test_prefill_path_small_layer_full_parity(M, act):
     # M > 128 with > 64 routes per expert: the tcgen05 path; M=1100 puts more

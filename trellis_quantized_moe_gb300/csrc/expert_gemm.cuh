@@ -325,25 +325,123 @@ struct Codebook {
     static constexpr uint32_t b = CB == EXL3_CB_3INST ? 64248484u : 0u;
 };
 
+// Per-lane word offsets and bit shift of the decode of one tile row: thread
+// (g, t) decodes, in every 16x16 tile, the two runs of 4 consecutive states
+// at positions 16g+4t.. (column g, run A) and 16(g+8)+4t.. (column g+8, run
+// B), whose windows start at the same bit offset modulo 32.
+template <int K>
+struct RowLanes {
+    int oA0, oA1, oA2, oB0, oB1, oB2, o;
+    __device__ __forceinline__ explicit RowLanes(int lane)
+    {
+        constexpr int NWD = 8 * K;                            // 32-bit words per tile
+        const int g = lane >> 2, t = lane & 3;
+        const int start = (16 * g + 4 * t + 1) * K - 16;      // first bit of run A's window
+        const int w0 = start >> 5;                            // floor (may be -1)
+        o = start & 31;
+        oA0 = (w0 + NWD) % NWD;
+        oA1 = (w0 + 1 + NWD) % NWD;
+        oA2 = (w0 + 2 + NWD) % NWD;
+        oB0 = (w0 + 4 * K) % NWD;
+        oB1 = (w0 + 4 * K + 1) % NWD;
+        oB2 = (w0 + 4 * K + 2) % NWD;
+    }
+};
+
+// Activation (B) fragments of one tk row for NRB 8-row groups: the 4 inputs
+// 16*tk + 4t.. of row g of each group, each fp16 duplicated into both halves
+// of a word (mcg/3inst: one MMA k element per weight half) or kept as pairs
+// (mul1).
+template <int CB, int NRB>
+__device__ __forceinline__ void load_bfrag(uint32_t (&bf)[NRB][4], const uint16_t *act, int ld,
+                                           int kcol)
+{
+    const int g = (threadIdx.x & 31) >> 2;
+#pragma unroll
+    for (int nb = 0; nb < NRB; nb++) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(act + (8 * nb + g) * ld + kcol);
+        if (CB == EXL3_CB_MUL1) {
+            bf[nb][0] = v.x;
+            bf[nb][1] = v.y;
+        } else {
+            bf[nb][0] = prmt(v.x, v.x, 0x1010);
+            bf[nb][1] = prmt(v.x, v.x, 0x3232);
+            bf[nb][2] = prmt(v.y, v.y, 0x1010);
+            bf[nb][3] = prmt(v.y, v.y, 0x3232);
+        }
+    }
+}
+
+// Decode one 16-input row of the 8 tiles of a 128-output block (row = its
+// 8 tiles' words in shared memory) and accumulate it into acc with mma.sync.
+template <int K, int CB, int NRB>
+__device__ __forceinline__ void decode_row(float (&acc)[NRB][8][4], const uint32_t *row,
+                                           const uint32_t (&bf)[NRB][4], const RowLanes<K> &rl,
+                                           const HashConsts &hc)
+{
+    constexpr int NWD = 8 * K;
+    constexpr bool W3 = 16 + 3 * K > 33;      // a run's window needs a third word (K >= 6)
+    constexpr bool MUL1 = CB == EXL3_CB_MUL1;
+    constexpr uint32_t mul = Codebook<CB>::a, add = Codebook<CB>::b;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const uint32_t *tw = row + j * NWD;
+        const uint32_t a0 = tw[rl.oA0], a1 = tw[rl.oA1];
+        const uint32_t b0 = tw[rl.oB0], b1 = tw[rl.oB1];
+        const uint32_t XA0 = __funnelshift_l(a1, a0, rl.o), XB0 = __funnelshift_l(b1, b0, rl.o);
+        uint32_t XA1 = 0, XB1 = 0;
+        if (W3) {
+            const uint32_t a2 = tw[rl.oA2], b2 = tw[rl.oB2];
+            XA1 = __funnelshift_l(a2, a1, rl.o);
+            XB1 = __funnelshift_l(b2, b1, rl.o);
+        }
+        uint32_t sA[4], sB[4];
+        sA[0] = run_state<K, 0>(XA0, XA1);
+        sA[1] = run_state<K, 1>(XA0, XA1);
+        sA[2] = run_state<K, 2>(XA0, XA1);
+        sA[3] = run_state<K, 3>(XA0, XA1);
+        sB[0] = run_state<K, 0>(XB0, XB1);
+        sB[1] = run_state<K, 1>(XB0, XB1);
+        sB[2] = run_state<K, 2>(XB0, XB1);
+        sB[3] = run_state<K, 3>(XB0, XB1);
+        if (MUL1) {
+            uint32_t dA[4], dB[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                dA[i] = __dp4a(sA[i] * mul, 0x01010101u, 0x6400u);
+                dB[i] = __dp4a(sB[i] * mul, 0x01010101u, 0x6400u);
+            }
+            const uint32_t A0 = hsub_1534(prmt(dA[0], dA[1], 0x5410));
+            const uint32_t A1 = hsub_1534(prmt(dB[0], dB[1], 0x5410));
+            const uint32_t A2 = hsub_1534(prmt(dA[2], dA[3], 0x5410));
+            const uint32_t A3 = hsub_1534(prmt(dB[2], dB[3], 0x5410));
+#pragma unroll
+            for (int nb = 0; nb < NRB; nb++)
+                mma_16816(acc[nb][j], A0, A1, A2, A3, bf[nb][0], bf[nb][1]);
+        } else {
+            uint32_t xA[4], xB[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                xA[i] = and_xor(sA[i] * mul + add, hc.mask, hc.flip);
+                xB[i] = and_xor(sB[i] * mul + add, hc.mask, hc.flip);
+            }
+#pragma unroll
+            for (int nb = 0; nb < NRB; nb++) {
+                mma_16816(acc[nb][j], xA[0], xB[0], xA[1], xB[1], bf[nb][0], bf[nb][1]);
+                mma_16816(acc[nb][j], xA[2], xB[2], xA[3], xB[3], bf[nb][2], bf[nb][3]);
+            }
+        }
+    }
+}
+
 // Decode + MMA over the warp's tk slice of one (chunk, pass).
 template <int K, int CB, int MODE, int NRB, bool ADD>
 __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
                                          const GemmArgs &a, int warp, const Pass &ps,
                                          int chunk, const uint16_t *act_s)
 {
-    constexpr int NWD = 8 * K;                // 32-bit words per tile
-    constexpr bool W3 = 16 + 3 * K > 33;      // a run's window needs a third word (K >= 6)
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int start = (16 * g + 4 * t + 1) * K - 16;   // first bit of run A's window
-    const int w0 = start >> 5;                          // floor (may be -1)
-    const int o = start & 31;
-    // word offsets (inside a tile) of the words of run A (column g) and run B
-    // (column g + 8, 128K bits later: same offset modulo 32)
-    const int oA0 = (w0 + NWD) % NWD, oA1 = (w0 + 1 + NWD) % NWD, oA2 = (w0 + 2 + NWD) % NWD;
-    const int oB0 = (w0 + 4 * K) % NWD, oB1 = (w0 + 4 * K + 1) % NWD, oB2 = (w0 + 4 * K + 2) % NWD;
-    constexpr bool MUL1 = CB == EXL3_CB_MUL1;
-    constexpr uint32_t mul = Codebook<CB>::a, add = Codebook<CB>::b;
-
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    const RowLanes<K> rl(lane);
     constexpr int RPS = rows_per_slot(K);
     const HashConsts hc = hash_consts(a.hdr);
     for (int tk_s = ps.tk0; tk_s < ps.tk1; tk_s += RPS) {
@@ -353,71 +451,9 @@ __device__ __forceinline__ void run_pass(float (&acc)[NRB][8][4], Ring &ring,
         for (int rr = 0; rr < nrows && seg != nullptr; rr++) {
             const int tk = tk_s + rr;
             const uint32_t *row = seg + rr * 64 * K;       // 8 tiles of 8K words
-            const int kcol = (tk - chunk * kChunkTk) * 16 + 4 * t;
             uint32_t bf[NRB][4];
-#pragma unroll
-            for (int nb = 0; nb < NRB; nb++) {
-                const uint2 v =
-                    *reinterpret_cast<const uint2 *>(act_s + (8 * nb + g) * kActLd + kcol);
-                if (MUL1) {
-                    bf[nb][0] = v.x;
-                    bf[nb][1] = v.y;
-                } else {
-                    bf[nb][0] = prmt(v.x, v.x, 0x1010);
-                    bf[nb][1] = prmt(v.x, v.x, 0x3232);
-                    bf[nb][2] = prmt(v.y, v.y, 0x1010);
-                    bf[nb][3] = prmt(v.y, v.y, 0x3232);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t *tw = row + j * NWD;
-                const uint32_t a0 = tw[oA0], a1 = tw[oA1];
-                const uint32_t b0 = tw[oB0], b1 = tw[oB1];
-                const uint32_t XA0 = __funnelshift_l(a1, a0, o), XB0 = __funnelshift_l(b1, b0, o);
-                uint32_t XA1 = 0, XB1 = 0;
-                if (W3) {
-                    const uint32_t a2 = tw[oA2], b2 = tw[oB2];
-                    XA1 = __funnelshift_l(a2, a1, o);
-                    XB1 = __funnelshift_l(b2, b1, o);
-                }
-                uint32_t sA[4], sB[4];
-                sA[0] = run_state<K, 0>(XA0, XA1);
-                sA[1] = run_state<K, 1>(XA0, XA1);
-                sA[2] = run_state<K, 2>(XA0, XA1);
-                sA[3] = run_state<K, 3>(XA0, XA1);
-                sB[0] = run_state<K, 0>(XB0, XB1);
-                sB[1] = run_state<K, 1>(XB0, XB1);
-                sB[2] = run_state<K, 2>(XB0, XB1);
-                sB[3] = run_state<K, 3>(XB0, XB1);
-                if (MUL1) {
-                    uint32_t dA[4], dB[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        dA[i] = __dp4a(sA[i] * mul, 0x01010101u, 0x6400u);
-                        dB[i] = __dp4a(sB[i] * mul, 0x01010101u, 0x6400u);
-                    }
-                    const uint32_t A0 = hsub_1534(prmt(dA[0], dA[1], 0x5410));
-                    const uint32_t A1 = hsub_1534(prmt(dB[0], dB[1], 0x5410));
-                    const uint32_t A2 = hsub_1534(prmt(dA[2], dA[3], 0x5410));
-                    const uint32_t A3 = hsub_1534(prmt(dB[2], dB[3], 0x5410));
-#pragma unroll
-                    for (int nb = 0; nb < NRB; nb++)
-                        mma_16816(acc[nb][j], A0, A1, A2, A3, bf[nb][0], bf[nb][1]);
-                } else {
-                    uint32_t xA[4], xB[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        xA[i] = and_xor(sA[i] * mul + add, hc.mask, hc.flip);
-                        xB[i] = and_xor(sB[i] * mul + add, hc.mask, hc.flip);
-                    }
-#pragma unroll
-                    for (int nb = 0; nb < NRB; nb++) {
-                        mma_16816(acc[nb][j], xA[0], xB[0], xA[1], xB[1], bf[nb][0], bf[nb][1]);
-                        mma_16816(acc[nb][j], xA[2], xB[2], xA[3], xB[3], bf[nb][2], bf[nb][3]);
-                    }
-                }
-            }
+            load_bfrag<CB, NRB>(bf, act_s, kActLd, (tk - chunk * kChunkTk) * 16 + 4 * t);
+            decode_row<K, CB, NRB>(acc, row, bf, rl, hc);
         }
         ring_release<MODE, NRB, ADD>(ring, a, warp);
     }
