@@ -119,6 +119,23 @@ def test_linear_prompt_rows_tcgen05(M, K, cb, act):
     assert_close_linear(y[rows], ref, act, f"linear tcgen05 M={M} K={K} cb={cb}")
 
 
+@pytest.mark.parametrize("M", [4900, 5220])
+def test_linear_paired_row_halves(M):
+    # more 256-row items than SMs: items of two 256-row halves share each
+    # decoded weight tile (4900 ends on a ragged second half, 5220 on an empty
+    # one); every row against the oracle, and the bytes equal those of a
+    # launch whose items hold one half
+    lw = LinearWorkload(M=M, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
+    dp = X.DeviceProjection(lw.proj)
+    y = _linear_gpu(lw, dp)
+    ref = O.linear(act_to_f64(lw.x, "bf16"), lw.proj)
+    assert_close_linear(to_f64(y), ref, "bf16", f"linear paired M={M}")
+    few = LinearWorkload(M=1024, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
+    few.x = lw.x[:1024]
+    y_few = _linear_gpu(few, dp).view(torch.int16).cpu().numpy()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy()[:1024], y_few)
+
+
 def test_linear_prompt_rows_do_not_depend_on_row_count():
     # above 128 rows every output column is computed by the same tcgen05
     # contraction whatever the tile's row count

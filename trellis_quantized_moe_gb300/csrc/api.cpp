@@ -466,7 +466,14 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
         if (!encode_act_maps(maps, ra.out, p->in_features, M, kTcKsDown))
             return EXL3_E_CUDA;
         g.split_host = 0;
-        g.n_items_host = ceil_div(M, tc_rows_per_item()) * L.nb;
+        // items of two 256-row halves decode each weight tile once for both
+        // and take ~5/3 the time of a one-half item (measured, 5120 -> 1536);
+        // they are used when that saves waves of SMs (M = 4096: 2 waves of
+        // one-half items -> 1 wave of pairs, -16%; 8192: 3 -> 2, +9%, kept)
+        const int items256 = ceil_div(M, tc_rows_per_item()) * L.nb;
+        const int items512 = ceil_div(M, 2 * tc_rows_per_item()) * L.nb;
+        g.lin_pair = 5 * ceil_div(items512, sms) < 3 * ceil_div(items256, sms) ? 1 : 0;
+        g.n_items_host = ceil_div(M, tc_rows_per_item() << g.lin_pair) * L.nb;
         const int grid = sms < g.n_items_host ? sms : g.n_items_host;
         return launch_tc_linear(g, maps, grid, stream) == cudaSuccess ? EXL3_OK : EXL3_E_CUDA;
     }

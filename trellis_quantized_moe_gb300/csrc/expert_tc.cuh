@@ -67,6 +67,9 @@ struct Traits {
     static constexpr int T = KS / 16;                            // trellis rows per stage
     static constexpr int SBO = (KS / 8) * 128;
     static constexpr int a_bytes = 128 * KS * 2;                 // per projection
+    // TMEM accumulator columns: routes per item x projections (linear: up to
+    // two 256-row halves of one decoded tile)
+    static constexpr int tmem_cols = (MODE == kModeLinear ? 2 : nproj) * kNT;
     // shared memory map
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + kStages * nproj * a_bytes;
@@ -112,6 +115,17 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     g.stage_bytes = NPROJ * g.proj_bytes;
     g.nslots = min(kMaxBSlots, kBRingBytes / g.stage_bytes);
     return g;
+}
+
+// Activation geometry of an item: as above, or for paired linear items two
+// 256-row boxes per stage (the second zero-filled past the last row).
+template <int MODE>
+__device__ __forceinline__ BGeom item_b_geom(const GemmArgs &a, int nrows)
+{
+    using T = Traits<MODE>;
+    if (MODE == kModeLinear && a.lin_pair)
+        return b_geom<T::KS, 2 * T::nproj>(kNT);
+    return b_geom<T::KS, T::nproj>(nrows);
 }
 
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
@@ -379,9 +393,10 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
     const int rgi = item / a.nb;
     it.nbk = item % a.nb;
     if (MODE == kModeLinear) {
+        const int rows = kNT << a.lin_pair;
         it.e = 0;
-        it.row0 = rgi * kNT;
-        it.nrows = min(kNT, a.M - it.row0);
+        it.row0 = rgi * rows;
+        it.nrows = min(rows, a.M - it.row0);
         return it;
     }
     const int4 r = static_cast<const int4 *>(a.rg)[rgi];
@@ -686,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_addr(tmem_slot)), "r"(T::nproj * kNT) : "memory");
+                     ::"r"(smem_addr(tmem_slot)), "r"(T::tmem_cols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     fence_before();
@@ -770,14 +785,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + T::off_b), 16 * T::KS, 2 * T::KS);
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
+                const BGeom bg = item_b_geom<MODE>(a, it.nrows);
                 if (bg.rb != cur_rb) {
                     bs = 0;
                     cur_rb = bg.rb;
                 }
                 const uint32_t bproj16 = bg.proj_bytes >> 4, bstage16 = bg.stage_bytes >> 4;
-                const int n_mma = max(16, (it.nrows + 15) & ~15);
-                const uint32_t idesc = instr_desc(n_mma);
+                // paired linear items: half h (rows 256h..) is B box h and
+                // TMEM columns 256h..; otherwise one half
+                const int nh = (MODE == kModeLinear && a.lin_pair) ? 2 : 1;
+                const int rows0 = min(it.nrows, kNT);
+                const uint32_t idesc = instr_desc(max(16, (rows0 + 15) & ~15));
+                const uint32_t idesc1 = instr_desc(max(16, (max(it.nrows - kNT, 0) + 15) & ~15));
                 if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
                     break;
                 fence_after();
@@ -809,6 +828,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                                         bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
                                         (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
                         }
+                        if (MODE == kModeLinear && nh == 2) {
+#pragma unroll
+                            for (int ks = 0; ks < T::KS / 16; ks++)
+                                mma_f16(tmem + kNT, ad + (uint32_t)(ks * 16),
+                                        bd + (uint32_t)(bproj16 + ks * 2), idesc1,
+                                        (s > 0 || ks > 0) ? 1u : 0u);
+                        }
                         mma_commit(&B.empty[slot]);
                         mma_commit(&B.bempty[bs]);
                         if (++bs == bg.nslots)
@@ -835,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items && !*abort; item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = b_geom<T::KS, T::nproj>(it.nrows);
+                const BGeom bg = item_b_geom<MODE>(a, it.nrows);
                 if (bg.rb != cur_rb) {
                     // slots of the old geometry overlap the new ones: drain the ring
                     for (int j = 0; ok && j < kMaxBSlots; j++)
@@ -857,6 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                         for (int p = 0; p < T::nproj; p++)
                             tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
                                         &B.bfull[bs]);
+                        if (MODE == kModeLinear && a.lin_pair)
+                            tma_load_2d(dst + bg.proj_bytes, map, s * T::KS, it.row0 + kNT, &B.bfull[bs]);
                     }
                 }
             }
@@ -965,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     if (warp == 1) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     ::"r"(tmem), "r"(T::nproj * kNT) : "memory");
+                     ::"r"(tmem), "r"(T::tmem_cols) : "memory");
     }
 }
 

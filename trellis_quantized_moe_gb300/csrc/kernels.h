@@ -62,8 +62,9 @@ struct GemmArgs {
     int in_f, out_f, nb, nchunks;
     int32_t *hdr;
     const void *rg;                 // int4 row groups (fused layer)
-    // linear: host-planned work
-    int M, n_items_host, split_host;
+    // linear: host-planned work; lin_pair: tcgen05 items of two 256-row
+    // halves sharing each decoded weight tile (two MMAs into 512 TMEM columns)
+    int M, n_items_host, split_host, lin_pair;
     const uint16_t *act;            // fp16 rows (rotated activations)
     long act_row_stride;            // halves between rows
     // gate/up of small decode-regime layers: rotate the raw activations x
