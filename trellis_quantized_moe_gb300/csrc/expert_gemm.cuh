@@ -12,7 +12,8 @@
 // Work item = (row group of <= 8*NRB routes of one expert, 128-output block,
 // range of 512-input chunks).  Each of the 8 warps owns a fixed slice of every
 // chunk, streams that slice's trellis words with cp.async.bulk into its own
-// 3-slot shared-memory ring (one mbarrier per slot), decodes each 16x16 tile
+// shared-memory ring of two 3 KB slots of whole tk rows (one mbarrier per
+// slot), decodes each 16x16 tile
 // in registers straight into mma.sync A fragments and multiplies by the rotated
 // activations (B fragments, rows = routes).
 //
