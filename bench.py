@@ -135,10 +135,12 @@ def _dist():
 
 
 def _max_over_ranks(dist, v):
+    """The slowest rank's time: every rank gets the maximum of v."""
     if dist is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
