@@ -312,6 +312,21 @@ def test_prefill_path_rows_do_not_depend_on_capacity():
     assert np.array_equal(a, b)
 
 
+def test_prefill_down_items_of_two_halves_match_row_groups():
+    # capacity <= 512: the down kernel's items are whole capacity tiles, two
+    # 256-route halves sharing each decoded tile when a tile holds more than
+    # 256 routes; capacity 2048: one item per row group of <= 256 routes.
+    # Same bytes either way (and with single-half tiles of <= 200 routes).
+    w = _small_layer(1100, "bf16", seed=1140)
+    assert np.bincount(w.ids.reshape(-1), minlength=8).min() > 256
+    ex = X.DeviceExperts.from_workload(w)
+    outs = []
+    for cap in (512, 2048, 200):
+        outs.append(run_layer(w, ex, capacity=cap).view(torch.int16).cpu().numpy())
+        assert LAST["regime"] == 1
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
 @pytest.mark.parametrize("cfg,M,regime", [(1, 136, 0), (3, 160, 1)])
 def test_regime_choice_above_128_tokens(cfg, M, regime):
     # both kernel pairs are launched above 128 tokens; the route-pack kernel

@@ -205,6 +205,9 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.capacity = capacity;
     rp.rg_size = 8 * nrb;
     rp.tc_rows = tc_ok ? tc_rows_per_item() : 0;
+    // prefill-regime down items: whole capacity tiles when a tile fits two
+    // 256-route halves (each decoded down tile then serves up to 512 routes)
+    rp.down_tiles = (tc_ok && capacity <= 2 * tc_rows_per_item()) ? 1 : 0;
     rp.cost_rg = 8 * nrb_plain;
     rp.dec_unit_cost = nrb_plain == 2 ? 1700 : 1050;
     rp.nw = route_pack_hist_warps(E, rp.R);
@@ -317,6 +320,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.rw_dtype = rw_dtype;
     g.cnt_comb = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = out;
+    g.tiles = rp.tiles;
+    g.down_tiles = rp.down_tiles;
     if ((tc_ok && launch_tc_down(g, maps2, sms, s) != cudaSuccess) ||
         launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess)
         return EXL3_E_CUDA;

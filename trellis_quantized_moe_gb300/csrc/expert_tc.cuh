@@ -67,9 +67,9 @@ struct Traits {
     static constexpr int T = KS / 16;                            // trellis rows per stage
     static constexpr int SBO = (KS / 8) * 128;
     static constexpr int a_bytes = 128 * KS * 2;                 // per projection
-    // TMEM accumulator columns: routes per item x projections (linear: up to
-    // two 256-row halves of one decoded tile)
-    static constexpr int tmem_cols = (MODE == kModeLinear ? 2 : nproj) * kNT;
+    // TMEM accumulator columns: gate and up x 256 routes, or (down, linear)
+    // up to two 256-row halves of one decoded tile
+    static constexpr int tmem_cols = 2 * kNT;
     // shared memory map
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + kStages * nproj * a_bytes;
@@ -117,13 +117,22 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     return g;
 }
 
-// Activation geometry of an item: as above, or for paired linear items two
+// Items of the down and linear modes may hold two 256-row halves that share
+// each decoded weight tile (two MMAs per k-step into TMEM columns 0-255 and
+// 256-511).
+template <int MODE>
+__device__ __forceinline__ int item_halves(int nrows)
+{
+    return (MODE != kModeGateUp && nrows > kNT) ? 2 : 1;
+}
+
+// Activation geometry of an item: as above, or for a two-half item two
 // 256-row boxes per stage (the second zero-filled past the last row).
 template <int MODE>
-__device__ __forceinline__ BGeom item_b_geom(const GemmArgs &a, int nrows)
+__device__ __forceinline__ BGeom item_b_geom(int nrows)
 {
     using T = Traits<MODE>;
-    if (MODE == kModeLinear && a.lin_pair)
+    if (item_halves<MODE>(nrows) == 2)
         return b_geom<T::KS, 2 * T::nproj>(kNT);
     return b_geom<T::KS, T::nproj>(nrows);
 }
@@ -397,6 +406,13 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
         it.e = 0;
         it.row0 = rgi * rows;
         it.nrows = min(rows, a.M - it.row0);
+        return it;
+    }
+    if (MODE == kModeDown && a.down_tiles) {
+        const int32_t *tl = a.tiles + 3 * rgi;
+        it.e = tl[0];
+        it.row0 = tl[1];
+        it.nrows = tl[2];
         return it;
     }
     const int4 r = static_cast<const int4 *>(a.rg)[rgi];
@@ -778,22 +794,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         if (lane == 0) {
             RingPos<kStages> ra;
             uint32_t nit = 0, bphase = 0;            // bphase: parity bit per B slot
-            int bs = 0, cur_rb = 0;                   // B ring slot, geometry
+            int bs = 0, cur_geom = 0;                 // B ring slot, geometry (stage bytes)
             // descriptors of A slot 0 / B ring byte 0; offsets are added in
             // 16-byte units to the address field
             const uint64_t adesc0 = smem_desc(smem_addr(smem + T::off_a), 128, T::SBO);
             const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + T::off_b), 16 * T::KS, 2 * T::KS);
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = item_b_geom<MODE>(a, it.nrows);
-                if (bg.rb != cur_rb) {
+                const BGeom bg = item_b_geom<MODE>(it.nrows);
+                if (bg.stage_bytes != cur_geom) {
                     bs = 0;
-                    cur_rb = bg.rb;
+                    cur_geom = bg.stage_bytes;
                 }
                 const uint32_t bproj16 = bg.proj_bytes >> 4, bstage16 = bg.stage_bytes >> 4;
                 // paired linear items: half h (rows 256h..) is B box h and
                 // TMEM columns 256h..; otherwise one half
-                const int nh = (MODE == kModeLinear && a.lin_pair) ? 2 : 1;
+                const int nh = item_halves<MODE>(it.nrows);
                 const int rows0 = min(it.nrows, kNT);
                 const uint32_t idesc = instr_desc(max(16, (rows0 + 15) & ~15));
                 const uint32_t idesc1 = instr_desc(max(16, (max(it.nrows - kNT, 0) + 15) & ~15));
@@ -828,12 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                                         bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
                                         (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
                         }
-                        if (MODE == kModeLinear && nh == 2) {
+                        if (MODE != kModeGateUp && nh == 2 && on[0]) {
 #pragma unroll
                             for (int ks = 0; ks < T::KS / 16; ks++)
                                 mma_f16(tmem + kNT, ad + (uint32_t)(ks * 16),
                                         bd + (uint32_t)(bproj16 + ks * 2), idesc1,
-                                        (s > 0 || ks > 0) ? 1u : 0u);
+                                        (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
                         }
                         mma_commit(&B.empty[slot]);
                         mma_commit(&B.bempty[bs]);
@@ -848,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         // ---------------- activation producer: 2D TMA boxes into the B ring
         if (lane == 0) {
             uint32_t pend = 0, ph = 0;                // per B slot: use in flight, parity
-            int bs = 0, cur_rb = 0;
+            int bs = 0, cur_geom = 0;
             auto reclaim = [&](int bs) -> bool {
                 if ((pend >> bs) & 1) {
                     if (!wait_bar(&B.bempty[bs], (ph >> bs) & 1, abort, a.hdr))
@@ -861,13 +877,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items && !*abort; item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = item_b_geom<MODE>(a, it.nrows);
-                if (bg.rb != cur_rb) {
+                const BGeom bg = item_b_geom<MODE>(it.nrows);
+                if (bg.stage_bytes != cur_geom) {
                     // slots of the old geometry overlap the new ones: drain the ring
                     for (int j = 0; ok && j < kMaxBSlots; j++)
                         ok = reclaim(j);
                     bs = 0;
-                    cur_rb = bg.rb;
+                    cur_geom = bg.stage_bytes;
                 }
                 const CUtensorMap *map = &maps.act[bg.map];
                 // the same activation tiles again for every residual pass
@@ -883,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                         for (int p = 0; p < T::nproj; p++)
                             tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
                                         &B.bfull[bs]);
-                        if (MODE == kModeLinear && a.lin_pair)
+                        if (item_halves<MODE>(it.nrows) == 2)
                             tma_load_2d(dst + bg.proj_bytes, map, s * T::KS, it.row0 + kNT, &B.bfull[bs]);
                     }
                 }

@@ -23,6 +23,8 @@ struct RoutePackArgs {
     // 1700).  A layer whose residual stages all have scale zero is the plain
     // forward, so the model never depends on the stages.
     int tc_rows, cost_rg, dec_unit_cost;
+    // prefill regime: the down kernel's items are the capacity tiles
+    int down_tiles;
     int32_t *offsets, *packed, *tiles, *info;
     int32_t *zero;                  // words to clear (per-call counters), or null
     int nzero;
@@ -87,6 +89,10 @@ struct GemmArgs {
     // split partials
     float *part;
     int32_t *cnt_split;
+    // prefill-regime down items are the capacity tiles (<= 512 routes, one or
+    // two 256-route halves) instead of the row groups
+    const int32_t *tiles;
+    int down_tiles;
     // outputs
     uint16_t *ad;                   // gate/up: fp16 [R][inter]
     float *stage;                   // down: fp32 [R][hidden]

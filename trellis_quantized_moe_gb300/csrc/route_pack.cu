@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
             a.info[kHdrSplit1] = split1;
             a.info[kHdrSplit2] = split2;
             a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
-            a.info[kHdrNItems2] = split2 ? pairs2 * a.nchunks2 : pairs2;
+            a.info[kHdrNItems2] = (use_tc && a.down_tiles) ? ntiles * a.nb2
+                                  : (split2 ? pairs2 * a.nchunks2 : pairs2);
             a.info[kHdrRegime] = use_tc ? 1 : 0;
         }
     }
