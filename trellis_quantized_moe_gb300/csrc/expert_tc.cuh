@@ -9,13 +9,16 @@
 // work run concurrently.
 //
 // Work item = (up to 256 routes of one expert, 128-output block); the whole
-// contraction runs in one CTA (one persistent CTA per SM).  Roles:
+// contraction runs in one CTA (one persistent CTA per SM).  Down items are
+// whole capacity tiles and linear items may pair two 256-row groups: up to
+// 512 routes as two halves sharing each decoded weight tile.  Roles:
 //   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 48 KB
 //               ring of stage slots sized by the layer's largest K (6 slots at
 //               K = 8, 12 at K = 4, 16 at K <= 3), mbarrier complete_tx,
 //               running into the next item as slots free up;
-//   warp 1      owns TMEM (gate and up accumulators: 128 lanes = outputs x
-//               256 columns = routes each); lane 0 issues tcgen05.mma
+//   warp 1      owns TMEM (512 columns: gate and up accumulators of 128
+//               lanes = outputs x 256 columns = routes each, or the two
+//               halves of a down / linear item); lane 0 issues tcgen05.mma
 //               (M=128, N=routes rounded up to 16, K=16) per stage and
 //               tcgen05.commit to release the stage's operands;
 //   warps 2-17  decode: each thread turns one 16-state trellis column run
