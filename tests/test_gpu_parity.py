@@ -371,12 +371,13 @@ def test_additive_layer_parity_and_zero_scale_identity():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("M", [24, 300])
+@pytest.mark.parametrize("M", [24, 300, 1100])
 def test_three_residual_stages_of_mixed_widths(M):
     # S = 4 (base + stages of K = 3, 1, 5, mcg, base rotations), some alpha
     # exactly 0, bases of all three codebooks (a mul1 base scales its mcg
     # residuals differently); above 128 tokens the tcgen05 kernels run the
-    # stages as extra passes over their accumulators
+    # stages as extra passes over their accumulators (1100 tokens: ~275
+    # routes per expert, so each down item is two 256-route halves)
     from workloads import MoESpec
     E = 8
     spec = MoESpec("stages", 512, 256, E, 2, M, "f16", "i32", "f32", np.full(E, 4),
