@@ -358,6 +358,7 @@ def run_ours(args):
         tm = float(np.mean(m_ms))
         b = _layer_bytes(wls[M], wls[M].ids)
         sweep[f"M={M}"] = {"us": 1e3 * tm, "tokens_per_s": M / (tm * 1e-3),
+                           "routes_per_s": M * spec.topk / (tm * 1e-3),
                            "layer_gbs": b / (tm * 1e-3) / 1e9,
                            "layer_frac_hbm": b / (tm * 1e-3) / 1e9 / hbm_peak,
                            "kernel_us": [1e3 * float(v) for v in m_kern.mean(axis=0)]}
@@ -431,6 +432,7 @@ def run_ours(args):
     prefill = {"workload": "hidden 5120, inter 1536, 192 experts, top-8, M=3072, K in {3,4} mcg, "
                            "Zipf(1.2) expert bias, capacity 512, bf16",
                "us": 1e3 * pt, "tokens_per_s": ps.M / (pt * 1e-3),
+               "routes_per_s": ps.M * ps.topk / (pt * 1e-3),
                "tflops_dense_equiv": flops / (pt * 1e-3) / 1e12,
                "frac_of_fp16_peak": flops / (pt * 1e-3) / 1e12 / bf16_peak,
                "peak_tflops": bf16_peak, "peak_note": f"bf16 burst ({peak_src}) x 1.0 fp16:bf16",
@@ -468,6 +470,7 @@ def run_ours(args):
                                " top-8, M=1, K=3 mcg, bf16 in/out, f16 MMA operands, f32 accumulate",
                    "M": 1, "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": f"replicas x{world}"},
+        "routes_per_s": world * spec.topk / (t_step_max * 1e-3),
         "layer_gbs": layer_bytes / (t_step_max * 1e-3) / 1e9,
         "layer_frac_hbm": layer_bytes / (t_step_max * 1e-3) / 1e9 / hbm_peak,
         "kernel_us": dict(zip(["route_pack", "rotate", "gate_up", "down_combine"],
