@@ -125,3 +125,23 @@ def test_residual_with_base_codes_and_unit_scale_doubles_the_weights():
     assert np.allclose(y2, O.linear(x, q), rtol=1e-12)
     y3 = O.linear(x, p, residuals=[(0.25, p.trellis, 3), (0.5, p.trellis, 3)])
     assert np.allclose(y3, 1.75 * O.linear(x, p), rtol=1e-12)
+
+
+@pytest.mark.parametrize("base_cb", [CB_MCG, CB_3INST, CB_MUL1])
+def test_residual_is_an_mcg_projection_with_the_base_rotations(base_cb):
+    # a stage adds alpha times the mcg projection of its own codes and width
+    # under the base's suh, svh and scale: the sum of two plain linears, each
+    # pinned on its own above
+    from workloads import Projection
+    p = make_projection([21, base_cb], 256, 384, 4, base_cb)
+    t2 = make_projection([22], 256, 384, 2, CB_MCG).trellis
+    t5 = make_projection([23], 256, 384, 5, CB_MCG).trellis
+    x = np.random.default_rng(24).standard_normal((5, 256))
+
+    def with_codes(trellis, K):
+        return Projection(trellis, p.suh, p.svh, p.scale, K, CB_MCG)
+
+    got = O.linear(x, p, residuals=[(0.3, t2, 2), (-0.125, t5, 5)])
+    want = (O.linear(x, p) + 0.3 * O.linear(x, with_codes(t2, 2))
+            - 0.125 * O.linear(x, with_codes(t5, 5)))
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
