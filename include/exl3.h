@@ -217,6 +217,12 @@ int exl3_moe_additive(const void *x, int act_dtype, int M, int hidden, int inter
 size_t exl3_linear_noalloc_max_scratch_bytes(void);
 int exl3_linear_noalloc(const void *x, int act_dtype, int M, const exl3_proj *proj, void *y,
                         cudaStream_t stream);
+/* The failure channel of exl3_linear_noalloc, whose workspace the caller never
+ * sees: waits for `stream`, then stores in *err_host the device error word
+ * (exl3_device_error bits, 0 = none) that the last exl3_linear_noalloc call on
+ * the current device left in the scratch.  Synchronises; never call it while
+ * the stream is capturing.  Returns EXL3_E_NULL for a null err_host. */
+int exl3_linear_noalloc_error(int32_t *err_host, cudaStream_t stream);
 
 /* Benchmark instrumentation: when `events` is non-NULL, the following calls of
  * exl3_moe_forward / exl3_moe_additive on this host thread record the five

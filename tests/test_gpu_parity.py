@@ -17,8 +17,8 @@ import trellis_quantized_moe_gb300 as X  # noqa: E402
 from oracle import exl3_oracle as O  # noqa: E402
 from workloads import (CB_3INST, CB_MCG, CB_MUL1, LinearWorkload, MoEWorkload,  # noqa: E402
                        act_to_f64, config)
-from gpu_common import (assert_close, assert_close_linear, moe_inputs, oracle_rows, out_tensor, to_device,  # noqa: E402
-                        to_f64)
+from gpu_common import (assert_close, assert_close_linear, covering_tokens, moe_inputs,  # noqa: E402
+                        oracle_rows, out_tensor, to_device, to_f64)
 
 
 # --------------------------------------------------------------------------- route pack
@@ -215,12 +215,11 @@ def test_tiny_layer_capacity_does_not_change_bytes():
         assert np.array_equal(o, outs[0])
 
 
-@pytest.mark.parametrize("M,tokens", [(1, None), (8, None), (32, [0, 13, 31]),
-                                      (128, [0, 64, 127])])
-def test_decode_layer_parity(M, tokens):
+@pytest.mark.parametrize("M,n", [(1, None), (8, None), (32, 8), (128, 8)])
+def test_decode_layer_parity(M, n):
     w = MoEWorkload(config(1, M=M))
     out = to_f64(run_layer(w, _experts(1)))
-    rows = np.arange(M) if tokens is None else np.array(tokens)
+    rows = np.arange(M) if n is None else covering_tokens(w, n, seed=M, cover=False)
     assert_close(out[rows], oracle_rows(w, tokens=rows), f"config 1 M={M}")
 
 
@@ -254,13 +253,15 @@ def test_layer_replayed_from_a_cuda_graph_matches_eager(cfg, M):
 
 
 def test_decode_layer_rows_byte_invariant_across_batch_sizes():
-    ref = None
+    # tokens are prefixes of one stream, so every row of the smaller batch is
+    # compared with the same row of the next larger one
+    prev = None
     for M in (1, 2, 8, 32, 128):
         w = MoEWorkload(config(1, M=M))
         o = run_layer(w, _experts(1)).view(torch.int16).cpu().numpy()
-        if ref is None:
-            ref = o
-        assert np.array_equal(o[:1], ref[:1]), M
+        if prev is not None:
+            assert np.array_equal(o[:prev.shape[0]], prev), M
+        prev = o
 
 
 def _small_layer(M, act, seed, E=8, topk=2):
@@ -342,7 +343,7 @@ def test_regime_choice_above_128_tokens(cfg, M, regime):
 def test_mixed_width_layer_parity():
     w = MoEWorkload(config(2))
     out = to_f64(run_layer(w, _experts(2)))
-    rows = np.array([0, 21, 63])
+    rows = covering_tokens(w, 32, seed=2, cover=False)
     assert_close(out[rows], oracle_rows(w, tokens=rows), "config 2")
 
 
@@ -350,7 +351,10 @@ def test_prefill_layer_parity_sampled():
     w = MoEWorkload(config(3))
     out = to_f64(run_layer(w, _experts(3)))
     assert LAST["regime"] == 1
-    rows = np.array([0, 1500, 3071])
+    # >= 64 tokens, with a checked route in every 256-route half of every
+    # capacity tile (the multi-tile spans of the Zipf-heavy experts included)
+    rows = covering_tokens(w, 64, seed=3)
+    assert len(rows) >= 64
     assert_close(out[rows], oracle_rows(w, tokens=rows), "config 3")
     assert np.all(np.isfinite(out))
 
@@ -361,7 +365,7 @@ def test_additive_layer_parity_and_zero_scale_identity():
     st = _stages(w)
     out = run_layer(w, ex, stages=st)
     assert LAST["regime"] == 1            # ~14 routes per expert: the tcgen05 kernels
-    rows = np.array([0, 255, 511])
+    rows = covering_tokens(w, 32, seed=4, cover=False)
     assert_close(to_f64(out)[rows], oracle_rows(w, tokens=rows), "config 4")
     # every stage at scale 0: bit-identical to the base-only forward
     zero = _stages(w)

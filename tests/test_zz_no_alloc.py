@@ -27,6 +27,16 @@ def _noalloc():
     return f, lib.exl3_linear_noalloc_max_scratch_bytes()
 
 
+def _noalloc_error(stream):
+    lib = X.binding.lib()
+    g = lib.exl3_linear_noalloc_error
+    g.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]
+    g.restype = ctypes.c_int
+    err = ctypes.c_int32(-1)
+    assert g(ctypes.byref(err), stream) == 0
+    return err.value
+
+
 def _with_workspace(lw, dp, x):
     y = torch.empty((lw.M, lw.proj.out_features), dtype=x.dtype, device="cuda")
     ws = torch.empty(X.exl3_linear_workspace_bytes(lw.M, lw.proj.in_features,
@@ -36,11 +46,14 @@ def _with_workspace(lw, dp, x):
     return y
 
 
-def test_noalloc_linear_matches_the_workspace_linear_on_consecutive_calls():
+@pytest.mark.parametrize("Ms", [(7, 3), (300, 256)])
+def test_noalloc_linear_matches_the_workspace_linear_on_consecutive_calls(Ms):
+    # (7, 3): the decode-regime kernel; (300, 256): prompt-sized rows, the
+    # tcgen05 kernel, whose activation tensor maps then point into the scratch
     f, cap = _noalloc()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    cases = [LinearWorkload(M=7, in_f=1408, out_f=4096, K=4, cb=CB_MCG, act="bf16", seed=31),
-             LinearWorkload(M=3, in_f=1408, out_f=4096, K=4, cb=CB_MCG, act="bf16", seed=32)]
+    cases = [LinearWorkload(M=Ms[0], in_f=1408, out_f=4096, K=4, cb=CB_MCG, act="bf16", seed=31),
+             LinearWorkload(M=Ms[1], in_f=1408, out_f=4096, K=4, cb=CB_MCG, act="bf16", seed=32)]
     cases[1].proj = cases[0].proj                  # same weights, new rows
     dp = X.DeviceProjection(cases[0].proj)
     st = dp.struct()
@@ -52,6 +65,7 @@ def test_noalloc_linear_matches_the_workspace_linear_on_consecutive_calls():
         rc = f(x.data_ptr(), X.EXL3_BF16, lw.M, ctypes.byref(st), y.data_ptr(), stream)
         assert rc == 0
         torch.cuda.synchronize()
+        assert _noalloc_error(stream) == 0
         assert_close_linear(to_f64(y), to_f64(ref), "bf16", "noalloc vs workspace")
         assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
 

@@ -67,4 +67,18 @@ int exl3_linear_noalloc(const void *x, int act_dtype, int M, const exl3_proj *pr
     return exl3_linear(x, act_dtype, M, proj, y, scratch, kNoAllocScratchBytes, stream);
 }
 
+// The device error word that the last exl3_linear_noalloc call on the current
+// device left in the fixed scratch (0: no device-side error).  Waits for the
+// stream, like exl3_workspace_error; never call it while capturing.
+int exl3_linear_noalloc_error(int32_t *err_host, cudaStream_t stream)
+{
+    if (!err_host)
+        return EXL3_E_NULL;
+    void *scratch = nullptr;
+    const int rc = scratch_for_current_device(&scratch);
+    if (rc != EXL3_OK)
+        return rc;
+    return exl3_workspace_error(scratch, err_host, stream);
+}
+
 }  // extern "C"
