@@ -204,7 +204,7 @@ def run_layer(w, experts, capacity=None, stages=None, ws=None):
 def test_tiny_layer_full_parity():
     w = MoEWorkload(config(0))
     out = to_f64(run_layer(w, _experts(0)))
-    assert_close(out, oracle_rows(w), "config 0")
+    assert_close(out, oracle_rows(w), w.spec.act, "config 0")
 
 
 def test_tiny_layer_capacity_does_not_change_bytes():
@@ -220,7 +220,7 @@ def test_decode_layer_parity(M, n):
     w = MoEWorkload(config(1, M=M))
     out = to_f64(run_layer(w, _experts(1)))
     rows = np.arange(M) if n is None else covering_tokens(w, n, seed=M, cover=False)
-    assert_close(out[rows], oracle_rows(w, tokens=rows), f"config 1 M={M}")
+    assert_close(out[rows], oracle_rows(w, tokens=rows), w.spec.act, f"config 1 M={M}")
 
 
 @pytest.mark.parametrize("cfg,M", [(1, 1), (1, 32), (0, 16)])
@@ -286,7 +286,7 @@ def test_small_layer_rows_byte_invariant_across_batch_sizes(act):
     b = run_layer(large, ex).view(torch.int16).cpu().numpy()
     assert np.array_equal(a, b[:16])
     got = to_f64(run_layer(small, ex))
-    assert_close(got, oracle_rows(small), f"16 tokens {act}")
+    assert_close(got, oracle_rows(small), act, f"16 tokens {act}")
 
 
 @pytest.mark.parametrize("M,act", [(512, "f16"), (1100, "bf16")])
@@ -337,14 +337,14 @@ def test_regime_choice_above_128_tokens(cfg, M, regime):
     out = to_f64(run_layer(w, _experts(cfg)))
     assert LAST["regime"] == regime
     rows = np.array([0, M // 2, M - 1])
-    assert_close(out[rows], oracle_rows(w, tokens=rows), f"config {cfg} M={M}")
+    assert_close(out[rows], oracle_rows(w, tokens=rows), w.spec.act, f"config {cfg} M={M}")
 
 
 def test_mixed_width_layer_parity():
     w = MoEWorkload(config(2))
     out = to_f64(run_layer(w, _experts(2)))
     rows = covering_tokens(w, 32, seed=2, cover=False)
-    assert_close(out[rows], oracle_rows(w, tokens=rows), "config 2")
+    assert_close(out[rows], oracle_rows(w, tokens=rows), w.spec.act, "config 2")
 
 
 def test_prefill_layer_parity_sampled():
@@ -355,7 +355,7 @@ def test_prefill_layer_parity_sampled():
     # capacity tile (the multi-tile spans of the Zipf-heavy experts included)
     rows = covering_tokens(w, 64, seed=3)
     assert len(rows) >= 64
-    assert_close(out[rows], oracle_rows(w, tokens=rows), "config 3")
+    assert_close(out[rows], oracle_rows(w, tokens=rows), w.spec.act, "config 3")
     assert np.all(np.isfinite(out))
 
 
@@ -366,7 +366,7 @@ def test_additive_layer_parity_and_zero_scale_identity():
     out = run_layer(w, ex, stages=st)
     assert LAST["regime"] == 1            # ~14 routes per expert: the tcgen05 kernels
     rows = covering_tokens(w, 32, seed=4, cover=False)
-    assert_close(to_f64(out)[rows], oracle_rows(w, tokens=rows), "config 4")
+    assert_close(to_f64(out)[rows], oracle_rows(w, tokens=rows), w.spec.act, "config 4")
     # every stage at scale 0: bit-identical to the base-only forward
     zero = _stages(w)
     zero.t_scale.zero_()
