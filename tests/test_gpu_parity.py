@@ -55,6 +55,11 @@ def test_route_pack_bit_exact_on_configs(cfg):
     (4000, 8, 1000, 7, "i64"),      # many experts, many warps
     (1, 1, 1, 1, "i32"),
     (0, 8, 16, 4, "i32"),           # empty batch
+    # at most 32 routes: the one-warp kernel
+    (1, 8, 192, 512, "i32"),        # one decode token over 192 experts
+    (4, 8, 192, 1, "i64"),          # capacity 1: every route its own tile
+    (31, 1, 3, 2, "i32"),           # 31 routes over 3 experts, multi-tile spans
+    (8, 4, 5, 3, "i64"),            # 32 routes, ragged tiles
 ])
 def test_route_pack_edge_cases(M, topk, E, cap, dt):
     rng = np.random.default_rng(M + E)
@@ -63,6 +68,8 @@ def test_route_pack_edge_cases(M, topk, E, cap, dt):
         ids[:, :] = np.arange(M * topk).reshape(M, topk) % 3
         ids[ids == 0] = 1
         ids.reshape(-1)[:cap + 1] = 0
+    if (M, topk) == (8, 4):
+        ids[2, :] = 4                   # one token listing an expert four times
     off, packed, tiles, info = _pack_on_gpu(ids, E, cap, dt)
     r_off, r_packed, r_tiles, r_nact = O.route_pack(ids, E, cap)
     assert np.array_equal(off, r_off) and np.array_equal(packed, r_packed)

@@ -58,7 +58,163 @@ __device__ __forceinline__ long long read_id(const IdT *ids, int f)
     return static_cast<long long>(ids[f]);
 }
 
+// The call's plan in the workspace header (one thread): tile, active-expert and
+// row-group counts, the contraction split of each decode-regime kernel and the
+// regime.  bad_table: an active expert's table entry is invalid.
+__device__ void write_plan_header(const RoutePackArgs &a, int ntiles, int nact, int n_rg, bool bad_table,
+                                  bool use_tc)
+{
+    a.info[kHdrNTiles] = ntiles;
+    a.info[kHdrNumActive] = nact;
+    if (!a.plan)
+        return;
+    if (bad_table) {
+        a.info[kHdrError] |= EXL3_DERR_TABLE;
+        n_rg = 0;
+    }
+    a.info[kHdrNRg] = n_rg;
+    const int pairs1 = n_rg * a.nb1, pairs2 = n_rg * a.nb2;
+    const int lim = min(kSplitMaxPairs, 4 * a.num_sms);
+    // the prefill regime never splits the contraction
+    const int split1 = !use_tc && a.nchunks1 > 1 && pairs1 <= min(lim, a.split_pairs1);
+    const int split2 = !use_tc && a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
+    a.info[kHdrSplit1] = split1;
+    a.info[kHdrSplit2] = split2;
+    a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
+    a.info[kHdrNItems2] = (use_tc && a.down_tiles) ? ntiles * a.nb2 : (split2 ? pairs2 * a.nchunks2 : pairs2);
+    a.info[kHdrRegime] = use_tc ? 1 : 0;
+}
+
+// Table entries of an active expert (the fused layer): widths, codebooks,
+// 16-/8-byte aligned non-null pointers, and every residual stage of nonzero
+// scale.  True when something is invalid.
+__device__ bool bad_tables(const RoutePackArgs &a, int e)
+{
+    int K[3], cb[3];
+    long long tr[3], su[3], sv[3], sc[3];
+#pragma unroll
+    for (int p = 0; p < 3; p++) {          // independent loads, issued together
+        const int i = e * 3 + p;
+        K[p] = a.t_K[i];
+        cb[p] = a.t_cb[i];
+        tr[p] = a.t_trellis[i];
+        su[p] = a.t_suh[i];
+        sv[p] = a.t_svh[i];
+        sc[p] = a.t_scale[i];
+    }
+    bool bad = false;
+#pragma unroll
+    for (int p = 0; p < 3; p++) {
+        bad |= (K[p] < 1) | (K[p] > 8) | (cb[p] < 0) | (cb[p] > 2) | (tr[p] == 0) |
+               ((tr[p] & 15) != 0) | (su[p] == 0) | ((su[p] & 7) != 0) | (sv[p] == 0) |
+               ((sv[p] & 7) != 0) | (sc[p] == 0) | ((sc[p] & 7) != 0);
+    }
+    for (int st = 1; st < a.num_stages; st++) {
+#pragma unroll
+        for (int p = 0; p < 3; p++) {
+            const int j = ((st - 1) * a.E + e) * 3 + p;
+            const float al = a.s_scale[j];
+            const int Ks = a.s_K[j];
+            const long long ts = a.s_trellis[j];
+            if (al != 0.0f)
+                bad |= (Ks < 1) | (Ks > 8) | (ts == 0) | ((ts & 15) != 0);
+        }
+    }
+    return bad;
+}
+
 }  // namespace
+
+// Layers of at most 32 routes (one decode step): one warp, no block barriers.
+// Lane f holds route f; __match_any_sync groups equal experts, the rank inside
+// a group is the count of lower lanes (the stable order), and every count,
+// offset and tile position is a sum over the other lanes by shuffles.  Same
+// outputs as k_route_pack.
+template <typename IdT>
+__global__ void __launch_bounds__(32, 1) k_route_pack_warp(RoutePackArgs a)
+{
+    const IdT *ids = static_cast<const IdT *>(a.ids);
+    const int E = a.E, R = a.R, lane = threadIdx.x;
+    for (int i = lane; i < a.nzero; i += 32)
+        a.zero[i] = 0;
+    const bool valid = lane < R;
+    const long long id = valid ? static_cast<long long>(ids[lane]) : -1;
+    if (lane == 0) {
+        a.info[kHdrError] = 0;
+        if (a.plan)
+            a.info[kHdrRegime] = 0;
+    }
+    if (__any_sync(0xffffffffu, valid && (id < 0 || id >= E))) {
+        if (lane == 0) {
+            a.info[kHdrError] |= EXL3_DERR_ROUTE_ID;
+            a.info[kHdrNTiles] = 0;
+            a.info[kHdrNumActive] = 0;
+            if (a.plan) {
+                a.info[kHdrNRg] = 0;
+                a.info[kHdrNItems1] = 0;
+                a.info[kHdrNItems2] = 0;
+            }
+        }
+        return;
+    }
+    const int e = valid ? static_cast<int>(id) : E;          // invalid lanes sort last
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    const unsigned peers = __match_any_sync(0xffffffffu, e) & vmask;
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int cnt = __popc(peers);
+    const bool leader = valid && rank == 0;                  // lowest lane of its expert
+    const int ntile_e = leader ? (cnt + a.capacity - 1) / a.capacity : 0;
+    int nrg_e = 0;
+    if (leader && a.plan)
+        for (int s0 = 0; s0 < cnt; s0 += a.capacity)
+            nrg_e += (min(a.capacity, cnt - s0) + a.rg_size - 1) / a.rg_size;
+    // position of this expert's span, tiles and row groups: sums over the
+    // routes / leaders of lower experts
+    int off_e = 0, tile_off = 0, rg_off = 0, ntiles = 0, n_rg = 0;
+    for (int f = 0; f < 32; f++) {
+        const int ef = __shfl_sync(0xffffffffu, e, f);
+        const int tf = __shfl_sync(0xffffffffu, ntile_e, f);
+        const int gf = __shfl_sync(0xffffffffu, nrg_e, f);
+        off_e += (f < R && ef < e) ? 1 : 0;
+        tile_off += ef < e ? tf : 0;
+        rg_off += ef < e ? gf : 0;
+        ntiles += tf;
+        n_rg += gf;
+    }
+    if (valid)
+        a.packed[off_e + rank] = lane;
+    // offsets[x] = routes with an expert below x, for every x in 0..E (the
+    // loop bounds are warp-uniform, so every lane takes part in each shuffle)
+    for (int x0 = 0; x0 <= E; x0 += 32) {
+        const int x = x0 + lane;
+        int c = 0;
+        for (int f = 0; f < R; f++)
+            c += __shfl_sync(0xffffffffu, e, f) < x ? 1 : 0;
+        if (x <= E)
+            a.offsets[x] = c;
+    }
+    const int nact = __popc(__ballot_sync(0xffffffffu, leader));
+    if (leader) {
+        for (int s0 = 0, t = 0; s0 < cnt; s0 += a.capacity, t++) {
+            int *tt = a.tiles + 3 * (tile_off + t);
+            tt[0] = e;
+            tt[1] = off_e + s0;
+            tt[2] = min(a.capacity, cnt - s0);
+        }
+        if (a.plan) {
+            int k = rg_off;
+            for (int s0 = 0; s0 < cnt; s0 += a.capacity) {
+                const int len = min(a.capacity, cnt - s0);
+                for (int r = 0; r < len; r += a.rg_size)
+                    static_cast<int4 *>(a.rg)[k++] = make_int4(e, off_e + s0 + r, min(a.rg_size, len - r), 0);
+            }
+        }
+    }
+    const bool bad = a.plan && leader && bad_tables(a, e);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0)
+        write_plan_header(a, ntiles, nact, n_rg, any_bad, false);
+}
 
 template <typename IdT>
 __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
@@ -227,64 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     }
 
     // the fused layer: validate the tables of every expert that receives routes
-    if (a.plan && tid < E && cnt > 0) {
-        int K[3], cb[3];
-        long long tr[3], su[3], sv[3], sc[3];
-#pragma unroll
-        for (int p = 0; p < 3; p++) {          // independent loads, issued together
-            const int i = tid * 3 + p;
-            K[p] = a.t_K[i];
-            cb[p] = a.t_cb[i];
-            tr[p] = a.t_trellis[i];
-            su[p] = a.t_suh[i];
-            sv[p] = a.t_svh[i];
-            sc[p] = a.t_scale[i];
-        }
-        bool bad = false;
-#pragma unroll
-        for (int p = 0; p < 3; p++) {
-            bad |= (K[p] < 1) | (K[p] > 8) | (cb[p] < 0) | (cb[p] > 2) | (tr[p] == 0) |
-                   ((tr[p] & 15) != 0) | (su[p] == 0) | ((su[p] & 7) != 0) | (sv[p] == 0) |
-                   ((sv[p] & 7) != 0) | (sc[p] == 0) | ((sc[p] & 7) != 0);
-        }
-        for (int s = 1; s < a.num_stages; s++) {
-#pragma unroll
-            for (int p = 0; p < 3; p++) {
-                const int j = ((s - 1) * E + tid) * 3 + p;
-                const float al = a.s_scale[j];
-                const int Ks = a.s_K[j];
-                const long long ts = a.s_trellis[j];
-                if (al != 0.0f)
-                    bad |= (Ks < 1) | (Ks > 8) | (ts == 0) | ((ts & 15) != 0);
-            }
-        }
-        if (bad)
-            s_err = 2;
-    }
+    if (a.plan && tid < E && cnt > 0 && bad_tables(a, tid))
+        s_err = 2;
     __syncthreads();
 
-    if (tid == 0) {
-        a.info[kHdrNTiles] = ntiles;
-        a.info[kHdrNumActive] = nact;
-        if (a.plan) {
-            if (s_err) {
-                a.info[kHdrError] |= EXL3_DERR_TABLE;
-                n_rg = 0;
-            }
-            a.info[kHdrNRg] = n_rg;
-            const int pairs1 = n_rg * a.nb1, pairs2 = n_rg * a.nb2;
-            const int lim = min(kSplitMaxPairs, 4 * a.num_sms);
-            // the prefill regime never splits the contraction
-            const int split1 = !use_tc && a.nchunks1 > 1 && pairs1 <= min(lim, a.split_pairs1);
-            const int split2 = !use_tc && a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
-            a.info[kHdrSplit1] = split1;
-            a.info[kHdrSplit2] = split2;
-            a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
-            a.info[kHdrNItems2] = (use_tc && a.down_tiles) ? ntiles * a.nb2
-                                  : (split2 ? pairs2 * a.nchunks2 : pairs2);
-            a.info[kHdrRegime] = use_tc ? 1 : 0;
-        }
-    }
+    if (tid == 0)
+        write_plan_header(a, ntiles, nact, n_rg, s_err != 0, use_tc);
 }
 
 // Warps holding a histogram row: at most 32, at most 16384 counters of shared
@@ -300,6 +404,14 @@ int route_pack_hist_warps(int E, int R)
 
 cudaError_t launch_route_pack(const RoutePackArgs &a, int ids_dtype, cudaStream_t s)
 {
+    if (a.R <= 32 && a.tc_rows == 0) {
+        // one decode step: the one-warp kernel (the regime is the decode one)
+        if (ids_dtype == EXL3_I64)
+            k_route_pack_warp<int64_t><<<1, 32, 0, s>>>(a);
+        else
+            k_route_pack_warp<int32_t><<<1, 32, 0, s>>>(a);
+        return cudaGetLastError();
+    }
     const size_t smem = (size_t)a.nw * a.E * sizeof(int);
     if (ids_dtype == EXL3_I64) {
         k_route_pack<int64_t><<<1, kThreads, smem, s>>>(a);
