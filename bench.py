@@ -4,10 +4,12 @@
 Headline: the decode-shaped layer (hidden 5120, inter 1536, 192 experts, top-8,
 K=3 mcg, bf16) at M=1 token: routed tokens/s of one layer call, with the L2
 flushed (256 MB write) before every timed step so the trellis words come from
-HBM.  The same line carries the M = 8 / 32 / 128 sweep, the M=3072 prefill
-layer (192 experts, K in {3,4}, Zipf-skewed routing), the roofline of the
-dominant kernel, an end-to-end figure through the C ABI with host buffers and
-the float64 CPU oracle timed on a bounded sample.
+HBM.  The same line carries the M = 8 / 32 / 128 sweep, the other layers of
+the five workloads (the 16-token tiny layer, the mixed-width 288-expert layer
+at M=64, the M=3072 prefill layer with Zipf-skewed routing, the additive
+residual layer at M=512), the HBM roofline of the dominant kernel, the
+prompt-sized linear, an end-to-end figure through the C ABI with host buffers
+and the float64 CPU oracle timed on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -196,6 +198,43 @@ def _gateup_bytes(w, ids):
     return trellis + vectors + R * 2 * s.hidden * 2 + R * s.inter * 2
 
 
+def _residual_bytes(w, ids):
+    """Trellis bytes of the residual stages with a nonzero scale, over the
+    experts the routes touch (the additive layer reads nothing else)."""
+    s = w.spec
+    total = 0
+    for st in range(1, s.num_stages):
+        K = int(s.residual_K[st - 1])
+        for e in np.unique(ids):
+            for p in range(3):
+                if w.alpha[st - 1, e, p] != 0.0:
+                    i, o = s.proj_shape(p)
+                    total += i * o * K // 8
+    return total
+
+
+def _fp16_peak(dev, n=8192, reps=10):
+    """Dense fp16 torch.matmul n^3 throughput (best of reps, CUDA events): the
+    tensor-core denominator of the prefill and linear fractions."""
+    import torch
+    a = torch.randn(n, n, dtype=torch.float16, device=dev)
+    b = torch.randn(n, n, dtype=torch.float16, device=dev)
+    for _ in range(2):
+        torch.matmul(a, b)
+    best = float("inf")
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
 def run_reference(args):
     """The float64 oracle on the host cores, each step one bounded sample."""
     from oracle import exl3_oracle as O
@@ -258,12 +297,19 @@ def run_ours(args):
     hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
     dev = torch.device("cuda", local_rank)
 
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+    def to_dev(a, dt):
+        if dt == "bf16":
+            return torch.from_numpy(a.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
     def dev_inputs(w):
         s = w.spec
-        x = torch.from_numpy(w.x.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-        ids = torch.from_numpy(w.ids).to(dev)
-        rw = torch.from_numpy(w.rw.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-        out = torch.empty((s.M, s.hidden), dtype=torch.bfloat16, device=dev)
+        x = to_dev(w.x, s.act)
+        ids = torch.from_numpy(w.ids.astype(np.int64 if s.ids_dtype == "i64" else np.int32)).to(dev)
+        rw = to_dev(w.rw, s.rw_dtype)
+        out = torch.empty((s.M, s.hidden), dtype=tdt[s.act], device=dev)
         return x, ids, rw, out
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -315,6 +361,37 @@ def run_ours(args):
                           "layer_gbs": _layer_bytes(w, w.ids) / (t * 1e-3) / 1e9,
                           "kernel_us": [1e3 * float(v) for v in kern.mean(axis=0)]}))
         return
+
+    def layer_case(cfg, name, steps, warmup, M=None):
+        """One workload's layer: mean step time without events between the
+        kernels, the per-kernel split from a separate profiled run, routed
+        tokens and routes per second, and the HBM view (algorithmic bytes of
+        the touched experts' trellis words, vectors and activations)."""
+        w = MoEWorkload(config(cfg, M=M))
+        s = w.spec
+        ex = X.DeviceExperts.from_workload(w)
+        st = (X.DeviceStages(w.residual, w.alpha, s.residual_K, s.E, device=dev)
+              if s.num_stages > 1 else None)
+        ws = torch.empty(X.exl3_moe_workspace_bytes(s.M, s.topk, s.E, s.hidden, s.inter, s.capacity),
+                         dtype=torch.uint8, device=dev)
+        x, ids, rw, out = dev_inputs(w)
+        if st is None:
+            call = lambda: X.exl3_moe_forward(x, ids, rw, ex, s.capacity, ws, out)  # noqa: E731
+        else:
+            call = lambda: X.exl3_moe_additive(x, ids, rw, ex, st, s.capacity, ws, out)  # noqa: E731
+        c_ms, _, _ = timed(call, steps, warmup)
+        _, c_kern, _ = timed(call, max(3, steps // 2), 1, profile=True)
+        assert X.exl3_workspace_error(ws) == 0
+        t = float(np.mean(c_ms))
+        b = _layer_bytes(w, w.ids) + (_residual_bytes(w, w.ids) if st is not None else 0)
+        res = {"workload": name, "M": s.M, "us": 1e3 * t, "tokens_per_s": s.M / (t * 1e-3),
+               "routes_per_s": s.M * s.topk / (t * 1e-3), "algorithmic_bytes": b,
+               "layer_gbs": b / (t * 1e-3) / 1e9, "layer_frac_hbm": b / (t * 1e-3) / 1e9 / hbm_peak,
+               "regime": "prefill (tcgen05)" if int(ws[:64 * 4].view(torch.int32)[8].item()) else "decode",
+               "kernel_us": [1e3 * float(v) for v in c_kern.mean(axis=0)]}
+        del ex, st, ws
+        torch.cuda.empty_cache()
+        return res
 
     # ---------------- decode-shaped layer (headline M=1 and the M sweep)
     base = MoEWorkload(config(1, M=1))
@@ -415,9 +492,24 @@ def run_ours(args):
     h2d = stage_h.numel()                       # the one staging copy, padding included
     d2h = out_h.numel() * out_h.element_size()
 
-    # ---------------- prefill layer, M = 3072
+    # ---------------- the other workloads
     del ex
     torch.cuda.empty_cache()
+    fp16_peak = _fp16_peak(dev)
+    n_cfg = max(5, min(20, args.steps // 2))
+    configs = {
+        "tiny_m16": layer_case(0, "hidden 512, inter 256, 8 experts, top-2, 16 tokens, K=4 mcg, f16",
+                               n_cfg, 3),
+        "mixed_width_m64": layer_case(2, "hidden 4096, inter 1408, 288 experts, top-8, M=64, K in 4..8 "
+                                         "per expert, 3inst (even) / mul1 (odd), f16, int64 ids",
+                                      n_cfg, 3),
+        "additive_m512": layer_case(4, "hidden 4096, inter 1408, 288 experts, top-8, M=512, base K=3 mcg "
+                                       "+ one K=2 mcg residual stage (50% of projections at scale 0), "
+                                       "bf16, int64 ids, f32 route weights",
+                                    max(3, n_cfg // 2), 2),
+    }
+
+    # ---------------- prefill layer, M = 3072
     pw = MoEWorkload(config(3))
     ps = pw.spec
     pex = X.DeviceExperts.from_workload(pw)
@@ -434,8 +526,10 @@ def run_ours(args):
                "us": 1e3 * pt, "tokens_per_s": ps.M / (pt * 1e-3),
                "routes_per_s": ps.M * ps.topk / (pt * 1e-3),
                "tflops_dense_equiv": flops / (pt * 1e-3) / 1e12,
-               "frac_of_fp16_peak": flops / (pt * 1e-3) / 1e12 / bf16_peak,
-               "peak_tflops": bf16_peak, "peak_note": f"bf16 burst ({peak_src}) x 1.0 fp16:bf16",
+               "frac_of_fp16_peak": flops / (pt * 1e-3) / 1e12 / fp16_peak,
+               "peak_tflops": fp16_peak,
+               "peak_note": "dense fp16 torch.matmul 8192^3, best of 10, measured in this run",
+               "frac_of_bf16_peak": flops / (pt * 1e-3) / 1e12 / bf16_peak,
                "layer_gbs": _layer_bytes(pw, pw.ids) / (pt * 1e-3) / 1e9,
                "kernel_us": [1e3 * float(v) for v in p_kern.mean(axis=0)]}
     del pex, pws
@@ -454,7 +548,7 @@ def run_ours(args):
     linear = {"workload": "EXL3 linear 5120 -> 1536, K=3 mcg, bf16, M=4096 rows",
               "us": 1e3 * lt, "rows_per_s": lw.M / (lt * 1e-3),
               "tflops_dense_equiv": lflops / (lt * 1e-3) / 1e12,
-              "frac_of_fp16_peak": lflops / (lt * 1e-3) / 1e12 / bf16_peak}
+              "frac_of_fp16_peak": lflops / (lt * 1e-3) / 1e12 / fp16_peak}
     del ldp, lws
     torch.cuda.empty_cache()
 
@@ -475,20 +569,24 @@ def run_ours(args):
         "layer_frac_hbm": layer_bytes / (t_step_max * 1e-3) / 1e9 / hbm_peak,
         "kernel_us": dict(zip(["route_pack", "rotate", "gate_up", "down_combine"],
                               [1e3 * float(v) for v in kmean])),
-        "roofline": {"kernel": "k_expert_gemm<gate/up>", "bound": "alu",
-                     "achieved": achieved_w / 1e9, "peak": alu_peak / 1e9, "unit": "Gweight/s",
-                     "frac": achieved_w / alu_peak, "traffic": _traffic("gate_up_m1"),
-                     "algorithmic_weights": gu_weights,
-                     "peak_source": f"derived: {nsm} SMs x {ALU_LANES_PER_SM} integer lanes/clk "
-                                    f"(ALU + FMA pipes) x {mhz:.0f} MHz / {ALU_OPS_PER_WEIGHT} "
-                                    f"integer ops per decoded weight",
-                     "hbm_view": {"achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                                  "frac": achieved / hbm_peak, "algorithmic_bytes": gu_bytes,
-                                  "peak_source": peak_src}},
+        # the dominant kernel against HBM on its algorithmic bytes (the
+        # metric's roofline); the integer-decode ceiling alongside
+        "roofline": {"kernel": "k_expert_gemm<gate/up> (decode regime, M=1)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": _traffic("gate_up_m1"),
+                     "algorithmic_bytes": gu_bytes, "peak_source": peak_src,
+                     "alu_view": {"achieved": achieved_w / 1e9, "peak": alu_peak / 1e9,
+                                  "unit": "Gweight/s", "frac": achieved_w / alu_peak,
+                                  "algorithmic_weights": gu_weights,
+                                  "peak_source": f"derived: {nsm} SMs x {ALU_LANES_PER_SM} integer "
+                                                 f"lanes/clk (ALU + FMA pipes) x {mhz:.0f} MHz / "
+                                                 f"{ALU_OPS_PER_WEIGHT} integer ops per decoded weight"}},
         "sweep": sweep,
         "graph_replay_m1": graph,
         "prefill_m3072": prefill,
+        "configs": configs,
         "linear_m4096": linear,
+        "fp16_dense_peak_tflops": fp16_peak,
         "e2e": {"value": world * 1 / (e_t * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
