@@ -127,11 +127,11 @@ def test_linear_prompt_rows_tcgen05(M, K, cb, act):
 
 
 @pytest.mark.parametrize("M", [4900, 5220])
-def test_linear_paired_row_halves(M):
-    # more 256-row items than SMs: items of two 256-row halves share each
-    # decoded weight tile (4900 ends on a ragged second half, 5220 on an empty
-    # one); every row against the oracle, and the bytes equal those of a
-    # launch whose items hold one half
+def test_linear_more_row_tiles_than_sms(M):
+    # more 256-row items than SMs (4900: 20 row tiles x 8 blocks, ragged last
+    # tile; 5220: a 100-row last tile): CTAs run several items, alternating
+    # between the two TMEM accumulators; every row against the oracle, and the
+    # bytes equal those of a launch with fewer items
     lw = LinearWorkload(M=M, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
     dp = X.DeviceProjection(lw.proj)
     y = _linear_gpu(lw, dp)
@@ -320,11 +320,11 @@ def test_prefill_path_rows_do_not_depend_on_capacity():
     assert np.array_equal(a, b)
 
 
-def test_prefill_down_items_of_two_halves_match_row_groups():
-    # capacity <= 512: the down kernel's items are whole capacity tiles, two
-    # 256-route halves sharing each decoded tile when a tile holds more than
-    # 256 routes; capacity 2048: one item per row group of <= 256 routes.
-    # Same bytes either way (and with single-half tiles of <= 200 routes).
+def test_prefill_rows_do_not_depend_on_row_group_boundaries():
+    # more than 256 routes per expert: capacity 512 cuts each expert's span
+    # into 256 + 256 + ... row groups, 2048 into 256-route groups from the
+    # span's start, 200 into groups of <= 200.  A route's bytes are the same
+    # in any group.
     w = _small_layer(1100, "bf16", seed=1140)
     assert np.bincount(w.ids.reshape(-1), minlength=8).min() > 256
     ex = X.DeviceExperts.from_workload(w)

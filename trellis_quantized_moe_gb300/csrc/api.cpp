@@ -113,20 +113,20 @@ EncodeTiledFn encode_tiled()
     return fn;
 }
 
-// fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box {ks, 16 << i}
-// with the swizzle of a ks * 2-byte row (64 or 128 bytes); rows past the end
+// fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box {kTcKs,
+// 16 << i} with the 128-byte swizzle of a 128-byte row; rows past the end
 // read as zero.
-bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows, int ks)
+bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows)
 {
     EncodeTiledFn fn = encode_tiled();
-    if (fn == nullptr || (ks != 32 && ks != 64))
+    if (fn == nullptr)
         return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapSwizzle swz = ks == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
     for (int i = 0; i < kTcMaps; i++) {
-        const cuuint32_t box[2] = {(cuuint32_t)ks, (cuuint32_t)(16 << i)};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcKs, (cuuint32_t)(16 << i)};
         if (fn(&m.act[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -205,9 +205,6 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     rp.capacity = capacity;
     rp.rg_size = 8 * nrb;
     rp.tc_rows = tc_ok ? tc_rows_per_item() : 0;
-    // prefill-regime down items: whole capacity tiles when a tile fits two
-    // 256-route halves (each decoded down tile then serves up to 512 routes)
-    rp.down_tiles = (tc_ok && capacity <= 2 * tc_rows_per_item()) ? 1 : 0;
     rp.cost_rg = 8 * nrb_plain;
     rp.dec_unit_cost = nrb_plain == 2 ? 1700 : 1050;
     rp.nw = route_pack_hist_warps(E, rp.R);
@@ -296,12 +293,15 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.part = reinterpret_cast<float *>(w + L.part1);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
     g.ad = reinterpret_cast<uint16_t *>(w + L.ad);
+    g.stage = reinterpret_cast<float *>(w + L.stage);
     TcMaps maps1, maps2;
-    if (tc_ok && (!encode_act_maps(maps1, g.act, 2 * hidden, R, kTcKsGateUp) ||
-                  !encode_act_maps(maps2, g.ad, inter, R, kTcKsDown)))
+    if (tc_ok && (!encode_act_maps(maps1, g.act, 2 * hidden, R) || !encode_act_maps(maps2, g.ad, inter, R)))
         return EXL3_E_CUDA;
+    // prefill regime: gate and up items stage their rotated outputs, then
+    // SwiGLU + the down-input rotation run as one elementwise pass
     if ((tc_ok && launch_tc_gateup(g, maps1, sms, s) != cudaSuccess) ||
-        launch_gemm_gateup(additive, nrb, g, sms * ctas, s) != cudaSuccess)
+        launch_gemm_gateup(additive, nrb, g, sms * ctas, s) != cudaSuccess ||
+        (tc_ok && launch_tc_gu_finish(g, sms, s) != cudaSuccess))
         return EXL3_E_CUDA;
     prof_mark(3, s);
 
@@ -314,16 +314,16 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     g.act_row_stride = inter;
     g.part = reinterpret_cast<float *>(w + L.part2);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt2);
-    g.stage = reinterpret_cast<float *>(w + L.stage);
     g.packed = rp.packed;
     g.rw = rw;
     g.rw_dtype = rw_dtype;
     g.cnt_comb = reinterpret_cast<int32_t *>(w + L.cnt);
     g.out = out;
-    g.tiles = rp.tiles;
-    g.down_tiles = rp.down_tiles;
+    // prefill regime: down items stage their rotated rows; the weighted
+    // combine follows as one pass in token order
     if ((tc_ok && launch_tc_down(g, maps2, sms, s) != cudaSuccess) ||
-        launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess)
+        launch_gemm_down(additive, nrb, g, sms * ctas, s) != cudaSuccess ||
+        (tc_ok && launch_tc_combine(g, sms, s) != cudaSuccess))
         return EXL3_E_CUDA;
     prof_mark(4, s);
     return EXL3_OK;
@@ -468,17 +468,10 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
         // 128 outputs, the whole contraction per item (M <= 128 keeps the
         // decode regime, so a row's bytes never depend on M there)
         TcMaps maps;
-        if (!encode_act_maps(maps, ra.out, p->in_features, M, kTcKsDown))
+        if (!encode_act_maps(maps, ra.out, p->in_features, M))
             return EXL3_E_CUDA;
         g.split_host = 0;
-        // items of two 256-row halves decode each weight tile once for both
-        // and take ~5/3 the time of a one-half item (measured, 5120 -> 1536);
-        // they are used when that saves waves of SMs (M = 4096: 2 waves of
-        // one-half items -> 1 wave of pairs, -16%; 8192: 3 -> 2, +9%, kept)
-        const int items256 = ceil_div(M, tc_rows_per_item()) * L.nb;
-        const int items512 = ceil_div(M, 2 * tc_rows_per_item()) * L.nb;
-        g.lin_pair = 5 * ceil_div(items512, sms) < 3 * ceil_div(items256, sms) ? 1 : 0;
-        g.n_items_host = ceil_div(M, tc_rows_per_item() << g.lin_pair) * L.nb;
+        g.n_items_host = ceil_div(M, tc_rows_per_item()) * L.nb;
         const int grid = sms < g.n_items_host ? sms : g.n_items_host;
         return launch_tc_linear(g, maps, grid, stream) == cudaSuccess ? EXL3_OK : EXL3_E_CUDA;
     }

@@ -1,46 +1,54 @@
 // Prefill-regime grouped GEMM on the 5th-generation tensor cores (tcgen05 +
-// TMEM), for the gate/up and down projections of the fused EXL3 MoE layer.
+// TMEM), for the gate/up and down projections of the fused EXL3 MoE layer and
+// for the prompt-sized linear.
 //
 // Follows "EXL3 linear and grouped routed experts" (TensorFold #837), "What this
 // changes" (trellis decode, grouped experts, gate and up, SwiGLU, down, the
 // weighted combine, a width per expert).  The pages' kernels decode into
 // mma.m16n8k16 fragments; on sm_103a the decoded tile goes to shared memory
-// and one thread drives tcgen05.mma, so the integer decode and the tensor
-// work run concurrently.
+// and one thread drives tcgen05.mma, so the integer decode, the tensor work
+// and the epilogue of the previous item run concurrently.
 //
-// Work item = (up to 256 routes of one expert, 128-output block); the whole
-// contraction runs in one CTA (one persistent CTA per SM).  Down items are
-// whole capacity tiles and linear items may pair two 256-row groups: up to
-// 512 routes as two halves sharing each decoded weight tile.  Roles:
-//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 48 KB
-//               ring of stage slots sized by the layer's largest K (6 slots at
-//               K = 8, 12 at K = 4, 16 at K <= 3), mbarrier complete_tx,
-//               running into the next item as slots free up;
-//   warp 1      owns TMEM (512 columns: gate and up accumulators of 128
-//               lanes = outputs x 256 columns = routes each, or the two
-//               halves of a down / linear item); lane 0 issues tcgen05.mma
-//               (M=128, N=routes rounded up to 16, K=16) per stage and
-//               tcgen05.commit to release the stage's operands;
-//   warps 2-17  decode: each thread turns one 16-state trellis column run
-//               (16 consecutive inputs of one output) into 16 fp16 weights
-//               (the two halves of the mcg/3inst word summed in fp16, mul1 as
-//               the exact integer byte sum - 510) and stores them, 16 bytes at
-//               a time, into a K-major no-swizzle A tile; after the last stage
-//               they read TMEM (tcgen05.ld), transpose 16 routes at a time
-//               through shared memory and run the per-row epilogues shared
-//               with the decode-regime kernel;
-//   warp 18     lane 0 loads the activation (B) tiles with 2D TMA into a byte
-//               ring that runs as far ahead of the MMAs as it has room.
-// Additive layers: each residual stage with a nonzero scale on some
-// projection of the item is one more pass of stages that every role walks
-// in the same order, accumulating into the same TMEM columns.
+// Work item = (up to 256 routes of one expert, 128-output block, one
+// projection): gate and up are separate items.  An item's accumulator takes
+// 256 TMEM columns (128 lanes = outputs x routes), so two items' accumulators
+// fit: while the epilogue warps drain one, the MMAs of the next fill the
+// other.  One persistent CTA per SM.  A stage covers 128 inputs: every
+// barrier wait, tcgen05.commit and activation copy then serves 8 MMAs (the
+// single issuing thread's own instruction latencies, not the tensor pipe,
+// bound 64-input stages).  Roles:
+//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 24 KB
+//               ring of word slots (4 rows each, two per stage) sized by the
+//               layer's largest K, mbarrier complete_tx, running into the
+//               next item as slots free up;
+//   warp 1      owns TMEM (2 x 256 columns); lane 0 issues tcgen05.mma
+//               (M=128, N=routes rounded up to 16, K=16) per stage into the
+//               item's buffer, tcgen05.commit to release the stage's
+//               operands, and at the item's end to hand the buffer over;
+//   warps 2-17  decode: each thread turns two 16-state trellis column runs
+//               (inputs 16t.. and 64+16t.. of one output) into 16 fp16
+//               weights each (the two halves of the mcg/3inst word summed in
+//               fp16, mul1 as the exact integer byte sum - 510) and stores
+//               them, 16 bytes at a time, into a K-major no-swizzle A tile;
+//   warp 18     lane 0 loads the activation (B) tiles with 2D TMA, two boxes
+//               per stage, into a byte ring that runs as far ahead of the
+//               MMAs as it has room;
+//   warps 19-22 epilogue: read the finished buffer (tcgen05.ld, one TMEM lane
+//               quarter each), transpose 16 routes at a time through shared
+//               memory and run the per-row output rotation: gate/up write
+//               Hb(z)*svh*scale in fp32 (the SwiGLU and the down-input
+//               rotation follow in k_tc_gu_finish), down writes its rotated
+//               rows to the fp32 staging (the weighted combine follows in
+//               k_tc_combine), the linear writes its output.
+// Additive layers: each residual stage with a nonzero scale on the item's
+// projection is one more pass of stages that every role walks in the same
+// order, accumulating into the same TMEM columns.
 // A layout (K-major, no swizzle): element (r, k) of a stage tile sits at
 // (r/8)*SBO + (k/8)*128 + (r%8)*16 + (k%8)*2 bytes, SBO = (KS/8)*128.
-// B layout (K-major, swizzled; one 2D TMA box {KS inputs, RB rows} per
-// projection and stage): route r's KS inputs are one 2*KS-byte row (64 bytes
-// with the 64-byte swizzle for gate/up, 128 with the 128-byte swizzle for
-// down), 8-row groups 16*KS bytes apart; the swizzle permutes the 16-byte
-// chunks of row r by r % 8 (64-byte: (r / 2) % 4) and is undone by the MMA.
+// B layout (K-major, 128-byte swizzle; two 2D TMA boxes {64 inputs, RB rows}
+// per stage, one after the other): route r's 64 inputs of a box are one
+// 128-byte row, 8-row groups 1 KB apart; the swizzle permutes the 16-byte
+// chunks of row r by r % 8 and is undone by the MMA.
 #pragma once
 #include <string.h>
 #include "common.cuh"
@@ -50,45 +58,42 @@
 namespace exl3 {
 namespace tc {
 
-constexpr int kNT = 256;          // routes per work item (MMA N upper bound)
-constexpr int kStages = 3;        // decoded-weight (A) stages
+constexpr int kNT = 256;          // routes per work item (MMA N upper bound), TMEM columns per buffer
+constexpr int kStages = 2;        // decoded-weight (A) stages
 constexpr int kTwSlots = 16;      // trellis word slots (at most; sized by the layer's largest K)
 constexpr int kBRingBytes = 128 * 1024;   // activation (B) stages, sized per item
 constexpr int kMaxBSlots = 16;
-constexpr int kTwRingBytes = 48 * 1024;
+constexpr int kTwRingBytes = 24 * 1024;
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kBWarp = 2 + kDecWarps;     // activation producer
-constexpr int kThreads = kDecThreads + 96;
-constexpr int kEpiRows = 32;      // routes per epilogue interval (2 per decode warp)
+constexpr int kEpiWarp0 = kBWarp + 1;     // first of four epilogue warps
+constexpr int kEpiThreads = 128;
+constexpr int kThreads = kDecThreads + 96 + kEpiThreads;
+constexpr int kEpiRows = 16;      // routes per epilogue interval
 constexpr int kZsLd = kHb + 4;
+constexpr int kKS = 2 * kTcKs;    // inputs per stage: two 64-input activation boxes
+constexpr int kT = kKS / 16;      // trellis rows per stage, in two word slots
+constexpr int kTH = kT / 2;       // trellis rows per word slot
 
-template <int MODE>
-struct Traits {
-    static constexpr int nproj = (MODE == kModeGateUp) ? 2 : 1;
-    static constexpr int KS = (MODE == kModeGateUp) ? kTcKsGateUp : kTcKsDown;   // inputs per stage
-    static constexpr int T = KS / 16;                            // trellis rows per stage
-    static constexpr int SBO = (KS / 8) * 128;
-    static constexpr int a_bytes = 128 * KS * 2;                 // per projection
-    // TMEM accumulator columns: gate and up x 256 routes, or (down, linear)
-    // up to two 256-row halves of one decoded tile
-    static constexpr int tmem_cols = 2 * kNT;
-    // shared memory map
+struct Smem {
+    static constexpr int SBO = (kKS / 8) * 128;
+    static constexpr int a_bytes = 128 * kKS * 2;               // one stage's A tile
+    static constexpr int tmem_cols = 2 * kNT;                   // two accumulator buffers
     static constexpr int off_a = 0;
-    static constexpr int off_b = off_a + kStages * nproj * a_bytes;
+    static constexpr int off_b = off_a + kStages * a_bytes;
     static constexpr int off_tw = off_b + kBRingBytes;
-    // epilogue staging reuses the A ring: it runs after the item's last MMA
-    // and before the next item's first decoded stage
-    static constexpr int off_zs = off_a;
-    static_assert(nproj * kEpiRows * kZsLd * 4 <= kStages * nproj * a_bytes, "staging fits the A ring");
-    static constexpr int off_bar = off_tw + kTwRingBytes;
-    static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 2;
+    static constexpr int off_zs = off_tw + kTwRingBytes;        // epilogue transpose, 16 routes
+    static constexpr int off_bar = off_zs + kEpiRows * kZsLd * 4;
+    static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 4;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int total = off_misc + 64;
 };
+static_assert(Smem::total <= 227 * 1024, "prefill kernel shared memory");
+static_assert(Smem::off_b % 1024 == 0, "128-byte swizzled B ring alignment");
 
 struct Bars {
-    uint64_t *full, *empty, *twfull, *twempty, *bfull, *bempty, *accfull, *accempty;
+    uint64_t *full, *empty, *twfull, *twempty, *bfull, *bempty, *tfull, *tempty;
 };
 
 // The activation tensor maps: one per TMA box height RB = 16, 32, ..., 256.
@@ -97,16 +102,14 @@ struct TcMapsDev {
 };
 
 // Activation ring geometry of one work item: RB = the item's routes rounded
-// up to a power of two (>= 16), one stage = nproj x KS/8 boxes of RB rows; as
-// many stages as fit in the ring (at most 16).  Items of the same geometry
-// continue one ring; a change of geometry first drains it.  (Rounding to a
-// power of two fetches about 5% more rows than rounding to 16 on a Zipf-routed
-// layer, and keeps one box per 8 inputs.)
+// up to a power of two (>= 16), one stage = one box of RB rows; as many stages
+// as fit in the ring (at most 16).  Items of the same geometry continue one
+// ring; a change of geometry first drains it.  (Rounding to a power of two
+// fetches about 5% more rows than rounding to 16 on a Zipf-routed layer.)
 struct BGeom {
-    int rb, map, proj_bytes, stage_bytes, nslots;
+    int rb, map, stage_bytes, nslots;
 };
 
-template <int KS, int NPROJ>
 __device__ __forceinline__ BGeom b_geom(int nrows)
 {
     BGeom g;
@@ -114,30 +117,9 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     while ((16 << g.map) < nrows)
         g.map++;
     g.rb = 16 << g.map;
-    g.proj_bytes = g.rb * KS * 2;
-    g.stage_bytes = NPROJ * g.proj_bytes;
+    g.stage_bytes = g.rb * kKS * 2;          // two boxes of rb rows x 128 bytes
     g.nslots = min(kMaxBSlots, kBRingBytes / g.stage_bytes);
     return g;
-}
-
-// Items of the down and linear modes may hold two 256-row halves that share
-// each decoded weight tile (two MMAs per k-step into TMEM columns 0-255 and
-// 256-511).
-template <int MODE>
-__device__ __forceinline__ int item_halves(int nrows)
-{
-    return (MODE != kModeGateUp && nrows > kNT) ? 2 : 1;
-}
-
-// Activation geometry of an item: as above, or for a two-half item two
-// 256-row boxes per stage (the second zero-filled past the last row).
-template <int MODE>
-__device__ __forceinline__ BGeom item_b_geom(int nrows)
-{
-    using T = Traits<MODE>;
-    if (item_halves<MODE>(nrows) == 2)
-        return b_geom<T::KS, 2 * T::nproj>(kNT);
-    return b_geom<T::KS, T::nproj>(nrows);
 }
 
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
@@ -158,6 +140,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
         }
     }
     return true;
+}
+
+// Warp-uniform forms for the roles whose 32 lanes run together (decode,
+// epilogue): every lane waits, and the warp goes on only if all lanes saw the
+// phase, so no lane is left behind at a warp-collective after a timeout.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                              int32_t *hdr)
+{
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, hdr));
+}
+
+__device__ __forceinline__ bool warp_aborted(volatile int *abort)
+{
+    return __any_sync(0xffffffffu, *abort != 0);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
@@ -349,10 +345,6 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar)
         mbar_arrive(bar);
 }
 
-struct TcItem {
-    int e, row0, nrows, nbk;
-};
-
 // Position in a ring of N slots: the slot and the parity of its current use
 // (flips whenever the slot index wraps).  A consumer waits for parity `phase`
 // on a slot's full barrier; a producer waits for `phase ^ 1` on its empty
@@ -396,26 +388,28 @@ __device__ __forceinline__ TwGeom tw_geom(int kmax)
     return g;
 }
 
-// Item = (row group, 128-output block).  Fused layer: row groups from the
-// route-pack plan (one expert's packed routes); linear: 256 token rows.
+struct TcItem {
+    int e, row0, nrows, nbk, p;   // p: gate (0) or up (1) of a gate/up item
+};
+
+// Item -> (row group, block, projection).  Fused layer: row groups of <= 256
+// routes from the route-pack plan (one expert's packed routes), gate and up
+// of one (row group, block) adjacent; linear: 256 token rows.
 template <int MODE>
 __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 {
     TcItem it;
+    it.p = 0;
+    if (MODE == kModeGateUp) {
+        it.p = item & 1;
+        item >>= 1;
+    }
     const int rgi = item / a.nb;
     it.nbk = item % a.nb;
     if (MODE == kModeLinear) {
-        const int rows = kNT << a.lin_pair;
         it.e = 0;
-        it.row0 = rgi * rows;
-        it.nrows = min(rows, a.M - it.row0);
-        return it;
-    }
-    if (MODE == kModeDown && a.down_tiles) {
-        const int32_t *tl = a.tiles + 3 * rgi;
-        it.e = tl[0];
-        it.row0 = tl[1];
-        it.nrows = tl[2];
+        it.row0 = rgi * kNT;
+        it.nrows = min(kNT, a.M - it.row0);
         return it;
     }
     const int4 r = static_cast<const int4 *>(a.rg)[rgi];
@@ -454,8 +448,8 @@ __device__ __forceinline__ ProjRef proj_ref(const GemmArgs &a, int e, int p)
 
 // Residual stages ("MoE: Add fused additive EXL3 kernels", exllamav3 #284,
 // "Summary"): pass 0 of an item is the base weights, pass s = 1..num_stages-1
-// residual stage s, included when some projection of the item has a nonzero
-// scale there.  Every role walks the same passes, stage by stage.
+// residual stage s, included when the item's projection has a nonzero scale
+// there.  Every role walks the same passes, stage by stage.
 template <int MODE>
 __device__ __forceinline__ int tc_num_passes(const GemmArgs &a)
 {
@@ -469,17 +463,6 @@ __device__ __forceinline__ float pass_alpha(const GemmArgs &a, int e, int p, int
     if (MODE == kModeLinear || s == 0)
         return 1.0f;
     return a.s_scale[((s - 1) * a.E + e) * 3 + proj_index<MODE>(p)];
-}
-
-template <int MODE>
-__device__ __forceinline__ bool pass_active(const GemmArgs &a, int e, int s)
-{
-    if (s == 0)
-        return true;
-    for (int p = 0; p < Traits<MODE>::nproj; p++)
-        if (pass_alpha<MODE>(a, e, p, s) != 0.0f)
-            return true;
-    return false;
 }
 
 // Trellis words, width and codebook of projection p in pass s (residuals are
@@ -506,71 +489,53 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 b)
 
 // All stages of one pass of a work item for one decode thread: trellis words
 // -> decoded A tile (times the pass's scale), one arrival per warp on the
-// stage barrier.  K and the codebook are compile-time.  A thread whose
-// projection sits this pass out (scale 0) keeps the barrier rhythm without
-// touching the trellis slot or its A tile.  RES: a residual pass (the base
-// pass compiles without the scale and the skip).
+// stage barrier.  K and the codebook are compile-time.  RES: a residual pass.
 template <int MODE, int K, int CB, bool RES>
 __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, const Bars &B,
-                                          volatile int *abort, const TcItem &it,
-                                          RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
-                                          int p, int t, int m, bool active, float alpha)
+                                          volatile int *abort, RingPos<kStages> &ra, RingPosN &rt,
+                                          const TwGeom &tg, int t, int m, float alpha)
 {
-    using T = Traits<MODE>;
-    const int nst = a.in_f / T::KS;
-    const bool act = !RES || active;
+    using S = Smem;
+    const int nst = a.in_f / kKS;
     const __half2 alpha2 = __float2half2_rn(alpha);
     const ColumnWindow<K> cw(m & 15);
     const HashConsts hc = hash_consts(a.hdr);
-    const int tile_off = (p * T::T + t) * tg.row_bytes + (m >> 4) * 32 * K;          // bytes
-    const int a_off = p * T::a_bytes + (m >> 3) * T::SBO + (m & 7) * 16 + 2 * t * 128;
-    // two stages per pass (the stage count is even): twice the independent
-    // decode work between barrier operations
-    for (int s = 0; s < nst; s += 2) {
-        RingPos<kStages> ra1 = ra;
+    const int tile_off = t * tg.row_bytes + (m >> 4) * 32 * K;          // bytes
+    const int a_off = (m >> 3) * S::SBO + (m & 7) * 16 + 2 * t * 128;
+    // one stage = two word slots (trellis rows t and t + 4 of this thread)
+    for (int s = 0; s < nst; s++) {
         RingPosN rt1 = rt;
-        ra1.next();
         rt1.next();
-        if (!wait_bar(&B.twfull[rt.slot], rt.phase, abort, a.hdr) ||
-            !wait_bar(&B.twfull[rt1.slot], rt1.phase, abort, a.hdr))
+        if (!warp_wait_bar(&B.twfull[rt.slot], rt.phase, abort, a.hdr) ||
+            !warp_wait_bar(&B.twfull[rt1.slot], rt1.phase, abort, a.hdr))
             return false;
         uint32_t w0[8], w1[8];
-        if (act) {
-            decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt.slot * tg.slot_bytes +
-                                                                    tile_off),
-                                 cw, hc, w0);
-            decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + T::off_tw + rt1.slot * tg.slot_bytes +
-                                                                    tile_off),
-                                 cw, hc, w1);
-            if (RES) {
+        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt.slot * tg.slot_bytes + tile_off),
+                             cw, hc, w0);
+        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt1.slot * tg.slot_bytes + tile_off),
+                             cw, hc, w1);
+        if (RES) {
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    w0[i] = hmul2_u32(w0[i], alpha2);
-                    w1[i] = hmul2_u32(w1[i], alpha2);
-                }
+            for (int i = 0; i < 8; i++) {
+                w0[i] = hmul2_u32(w0[i], alpha2);
+                w1[i] = hmul2_u32(w1[i], alpha2);
             }
         }
         warp_arrive(&B.twempty[rt.slot]);
         warp_arrive(&B.twempty[rt1.slot]);
-        // an A slot is free once the MMA of its previous stage completed; the
+        // an A slot is free once the MMAs of its previous stage completed; the
         // decode above does not need it
-        if (!wait_bar(&B.empty[ra.slot], ra.phase ^ 1, abort, a.hdr) ||
-            !wait_bar(&B.empty[ra1.slot], ra1.phase ^ 1, abort, a.hdr))
+        if (!warp_wait_bar(&B.empty[ra.slot], ra.phase ^ 1, abort, a.hdr))
             return false;
-        uint8_t *abuf0 = smem + T::off_a + ra.slot * T::nproj * T::a_bytes + a_off;
-        uint8_t *abuf1 = smem + T::off_a + ra1.slot * T::nproj * T::a_bytes + a_off;
-        if (act) {
-            *reinterpret_cast<uint4 *>(abuf0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            *reinterpret_cast<uint4 *>(abuf0 + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-            *reinterpret_cast<uint4 *>(abuf1) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            *reinterpret_cast<uint4 *>(abuf1 + 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-        }
+        uint8_t *abuf = smem + S::off_a + ra.slot * S::a_bytes + a_off;
+        *reinterpret_cast<uint4 *>(abuf) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4 *>(abuf + 128) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+        *reinterpret_cast<uint4 *>(abuf + 8 * 128) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        *reinterpret_cast<uint4 *>(abuf + 9 * 128) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         warp_arrive(&B.full[ra.slot]);
-        warp_arrive(&B.full[ra1.slot]);
-        ra1.next();
+        ra.next();
         rt1.next();
-        ra = ra1;
         rt = rt1;
     }
     return true;
@@ -578,53 +543,50 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
 
 template <int MODE, int K>
 __device__ __forceinline__ bool tc_stages_cb(int cb, const GemmArgs &a, uint8_t *smem, const Bars &B,
-                                             volatile int *abort, const TcItem &it,
-                                             RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
-                                             int p, int t, int m)
+                                             volatile int *abort, RingPos<kStages> &ra, RingPosN &rt,
+                                             const TwGeom &tg, int t, int m)
 {
     if (cb == EXL3_CB_MUL1)
-        return tc_stages<MODE, K, EXL3_CB_MUL1, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
+        return tc_stages<MODE, K, EXL3_CB_MUL1, false>(a, smem, B, abort, ra, rt, tg, t, m, 1.0f);
     if (cb == EXL3_CB_3INST)
-        return tc_stages<MODE, K, EXL3_CB_3INST, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
-    return tc_stages<MODE, K, EXL3_CB_MCG, false>(a, smem, B, abort, it, ra, rt, tg, p, t, m, true, 1.0f);
+        return tc_stages<MODE, K, EXL3_CB_3INST, false>(a, smem, B, abort, ra, rt, tg, t, m, 1.0f);
+    return tc_stages<MODE, K, EXL3_CB_MCG, false>(a, smem, B, abort, ra, rt, tg, t, m, 1.0f);
 }
 
 // One decode thread's share of one work item: the base pass, then each
-// residual pass of the item.  A mul1 base is scaled by 1/sqrt(21845) in the
-// epilogue while the (mcg) residuals are not, so their scale carries
-// sqrt(21845) for such a projection.
+// residual pass of the item's projection.  A mul1 base is scaled by
+// 1/sqrt(21845) in the epilogue while the (mcg) residuals are not, so their
+// scale carries sqrt(21845) for such a projection.
 template <int MODE>
 __device__ __forceinline__ bool tc_item_decode(const GemmArgs &a, uint8_t *smem, const Bars &B,
                                                volatile int *abort, const TcItem &it,
                                                RingPos<kStages> &ra, RingPosN &rt, const TwGeom &tg,
-                                               int p, int t, int m)
+                                               int t, int m)
 {
-    const ProjRef base = proj_ref<MODE>(a, it.e, p);
+    const ProjRef base = proj_ref<MODE>(a, it.e, it.p);
     bool ok;
     switch (base.K) {
-        case 1: ok = tc_stages_cb<MODE, 1>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 2: ok = tc_stages_cb<MODE, 2>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 3: ok = tc_stages_cb<MODE, 3>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 4: ok = tc_stages_cb<MODE, 4>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 5: ok = tc_stages_cb<MODE, 5>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 6: ok = tc_stages_cb<MODE, 6>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        case 7: ok = tc_stages_cb<MODE, 7>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
-        default: ok = tc_stages_cb<MODE, 8>(base.cb, a, smem, B, abort, it, ra, rt, tg, p, t, m); break;
+        case 1: ok = tc_stages_cb<MODE, 1>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 2: ok = tc_stages_cb<MODE, 2>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 3: ok = tc_stages_cb<MODE, 3>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 4: ok = tc_stages_cb<MODE, 4>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 5: ok = tc_stages_cb<MODE, 5>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 6: ok = tc_stages_cb<MODE, 6>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        case 7: ok = tc_stages_cb<MODE, 7>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
+        default: ok = tc_stages_cb<MODE, 8>(base.cb, a, smem, B, abort, ra, rt, tg, t, m); break;
     }
-    if (!ok || *abort)
+    if (!ok || warp_aborted(abort))
         return false;
     const int npass = tc_num_passes<MODE>(a);
     for (int s = 1; s < npass; s++) {
-        if (!pass_active<MODE>(a, it.e, s))
+        const float al = pass_alpha<MODE>(a, it.e, it.p, s);
+        if (al == 0.0f)
             continue;
-        const float al = pass_alpha<MODE>(a, it.e, p, s);
-        const bool active = al != 0.0f;
-        const int K = active ? pass_ref<MODE>(a, it.e, p, s).K : 1;
+        const int K = pass_ref<MODE>(a, it.e, it.p, s).K;
         const float alpha = base.cb == EXL3_CB_MUL1 ? al * kSqrtMul1 : al;
-#define EXL3_RES_CASE(KK)                                                                        \
-    case KK:                                                                                     \
-        ok = tc_stages<MODE, KK, EXL3_CB_MCG, true>(a, smem, B, abort, it, ra, rt, tg, p, t, m,  \
-                                                    active, alpha);                              \
+#define EXL3_RES_CASE(KK)                                                                            \
+    case KK:                                                                                         \
+        ok = tc_stages<MODE, KK, EXL3_CB_MCG, true>(a, smem, B, abort, ra, rt, tg, t, m, alpha);     \
         break;
         switch (K) {
             EXL3_RES_CASE(1)
@@ -635,50 +597,107 @@ __device__ __forceinline__ bool tc_item_decode(const GemmArgs &a, uint8_t *smem,
             EXL3_RES_CASE(6)
             EXL3_RES_CASE(7)
             default:
-                ok = tc_stages<MODE, 8, EXL3_CB_MCG, true>(a, smem, B, abort, it, ra, rt, tg, p, t, m,
-                                                           active, alpha);
+                ok = tc_stages<MODE, 8, EXL3_CB_MCG, true>(a, smem, B, abort, ra, rt, tg, t, m, alpha);
                 break;
         }
 #undef EXL3_RES_CASE
-        if (!ok || *abort)
+        if (!ok || warp_aborted(abort))
             return false;
     }
     return true;
 }
 
+// Output rotation of one route row of a gate/up item (lane l owns outputs
+// 4l..4l+3 of the block): Hb(z)*svh*scale in fp32, into the staging row of the
+// packed route (gate at columns 0..inter, up at inter..2*inter); k_gu_finish
+// takes it from there.
+__device__ __forceinline__ void epi_gu_half_row(const GemmArgs &a, const DownConsts &c, int p, int nbk, int prow,
+                                                float z[4])
+{
+    const int lane = threadIdx.x & 31;
+    warp_hadamard128(z);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        z[i] = z[i] * kInvSqrt128 * c.sv[i] * c.sc[i];
+    *reinterpret_cast<float4 *>(a.stage + (size_t)prow * (2 * a.out_f) + p * a.out_f + nbk * kHb + 4 * lane) =
+        make_float4(z[0], z[1], z[2], z[3]);
+}
+
+// The epilogue warps' share of one item: buffer `buf` of TMEM -> 16 routes at
+// a time through shared memory -> per-row output rotation.  Warp ew (0..3)
+// reads TMEM lane quarter q = its warp index % 4 and runs routes ew*4..ew*4+3
+// of each interval.
+template <int MODE>
+__device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem &it, uint32_t tbuf, float *zs,
+                                                 int ew, int q)
+{
+    const int lane = threadIdx.x & 31;
+    DownConsts cd;
+    const int pi = proj_index<MODE>(it.p);
+    if (MODE == kModeLinear) {
+        epi_linear_consts(a, it.nbk, cd);
+    } else {
+        const int col = it.nbk * kHb + 4 * lane;
+        load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[it.e * 3 + pi]), col, cd.sv);
+        load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[it.e * 3 + pi]), col, cd.sc);
+    }
+    const float fac = (proj_ref<MODE>(a, it.e, it.p).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+    for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
+        uint32_t v[16];
+        tmem_ld<16>(tbuf + ((uint32_t)(32 * q) << 16) + r0, v);
+#pragma unroll
+        for (int j = 0; j < 16; j++)
+            zs[j * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac;
+        named_barrier(2, kEpiThreads);
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            const int rr = 4 * ew + h, r = r0 + rr;
+            if (r < it.nrows) {
+                float z[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    z[i] = zs[rr * kZsLd + 4 * lane + i];
+                if (MODE == kModeGateUp)
+                    epi_gu_half_row(a, cd, it.p, it.nbk, it.row0 + r, z);
+                else if (MODE == kModeLinear)
+                    epi_linear_row(a, cd, it.nbk, it.row0 + r, z);
+                else
+                    epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
+            }
+        }
+        named_barrier(2, kEpiThreads);
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __grid_constant__ TcMapsDev maps)
 {
-    using T = Traits<MODE>;
+    using S = Smem;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Bars B;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::off_bar);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::off_bar);
     B.full = bars;
     B.empty = bars + kStages;
     B.twfull = bars + 2 * kStages;
     B.twempty = bars + 2 * kStages + kTwSlots;
     B.bfull = bars + 2 * kStages + 2 * kTwSlots;
     B.bempty = B.bfull + kMaxBSlots;
-    B.accfull = B.bempty + kMaxBSlots;
-    B.accempty = B.accfull + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::off_misc);
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + T::off_misc + 8);
-    int *kmax_slot = reinterpret_cast<int *>(smem + T::off_misc + 16);
+    B.tfull = B.bempty + kMaxBSlots;           // [2]
+    B.tempty = B.tfull + 2;                    // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::off_misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::off_misc + 8);
+    int *kmax_slot = reinterpret_cast<int *>(smem + S::off_misc + 16);
 
     if (MODE != kModeLinear && a.hdr[kHdrRegime] != 1)
         return;                              // the decode-regime kernels run this layer
     const int n_items = MODE == kModeLinear ? a.n_items_host
                                             : a.hdr[MODE == kModeGateUp ? kHdrNItems1 : kHdrNItems2];
-    if (MODE == kModeDown && a.hdr[kHdrError] != 0) {
-        const size_t n = (size_t)a.M_tokens * a.out_f;
-        for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < n; i += (size_t)gridDim.x * kThreads)
-            reinterpret_cast<uint16_t *>(a.out)[i] = 0;
-        return;
-    }
+    if (MODE == kModeDown && a.hdr[kHdrError] != 0)
+        return;                              // k_tc_combine writes zeros
     if ((int)blockIdx.x >= n_items)
         return;
-    const int nst = a.in_f / T::KS;                 // stages per item
+    const int nst = a.in_f / kKS;                   // stages per item
     const int ntn = a.out_f / 16;
 
     if (tid == 0) {
@@ -694,8 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             mbar_init(&B.bfull[s], 1);
             mbar_init(&B.bempty[s], 1);
         }
-        mbar_init(B.accfull, 1);
-        mbar_init(B.accempty, kDecWarps);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&B.tfull[b], 1);
+            mbar_init(&B.tempty[b], kEpiThreads / 32);
+        }
         *abort = 0;
         fence_mbar_init();
     }
@@ -706,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             km = max(1, min(8, a.lin.K));
         else
             for (int e = lane; e < a.E; e += 32)
-                for (int p = 0; p < T::nproj; p++) {
+                for (int p = 0; p < (MODE == kModeGateUp ? 2 : 1); p++) {
                     km = max(km, min(8, a.t_K[e * 3 + proj_index<MODE>(p)]));
                     for (int st = 1; st < tc_num_passes<MODE>(a); st++)
                         if (pass_alpha<MODE>(a, e, p, st) != 0.0f)
@@ -720,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_addr(tmem_slot)), "r"(T::tmem_cols) : "memory");
+                     ::"r"(smem_addr(tmem_slot)), "r"(S::tmem_cols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     fence_before();
@@ -734,62 +755,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         if (lane == 0) {
             RingPosN rt;
             rt.n = tg.nslots;
-            // trellis rows of one pass of an item: first row of each projection's
-            // 128-output block, K per projection, bytes per stage (projections
-            // with scale 0 in the pass stream nothing)
-            struct Src {
-                const uint32_t *tr[2];
-                int K[2];
-                bool on[2];
-                uint32_t bytes;
-            };
-            auto src_of = [&](const TcItem &it, int ps) {
-                Src r;
-                r.bytes = 0;
-                for (int p = 0; p < T::nproj; p++) {
-                    r.on[p] = pass_alpha<MODE>(a, it.e, p, ps) != 0.0f;
-                    r.K[p] = 1;
-                    r.tr[p] = nullptr;
-                    if (!r.on[p])
-                        continue;
-                    const ProjRef pr = pass_ref<MODE>(a, it.e, p, ps);
-                    r.K[p] = pr.K;
-                    r.tr[p] = pr.trellis + (size_t)it.nbk * 8 * (8 * r.K[p]);
-                    r.bytes += T::T * 256 * r.K[p];
-                }
-                return r;
-            };
-            auto row_of = [&](const Src &r, int p, int tk) { return r.tr[p] + (size_t)tk * ntn * (8 * r.K[p]); };
-            // (no separate L2 prefetch: measured slower, its requests compete
-            // with the ring's own copies)
             const int npass = tc_num_passes<MODE>(a);
-            int item = blockIdx.x;
-            TcItem cit = tc_item<MODE>(a, item);
-            Src cur = src_of(cit, 0);
-            for (; item < n_items && !*abort; item += gridDim.x) {
-                // the next item's base rows are looked up while this one streams
-                const int next = item + (int)gridDim.x;
-                const TcItem nit = next < n_items ? tc_item<MODE>(a, next) : cit;
-                const Src nxt = next < n_items ? src_of(nit, 0) : cur;
+            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
+                const TcItem it = tc_item<MODE>(a, item);
                 for (int ps = 0; ps < npass && !*abort; ps++) {
-                    if (ps > 0 && !pass_active<MODE>(a, cit.e, ps))
+                    if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
                         continue;
-                    const Src sp = ps == 0 ? cur : src_of(cit, ps);
-                    for (int s = 0; s < nst; s++, rt.next()) {
+                    const ProjRef pr = pass_ref<MODE>(a, it.e, it.p, ps);
+                    const uint32_t *tr0 = pr.trellis + (size_t)it.nbk * 8 * (8 * pr.K);
+                    const uint32_t bytes = kTH * 256 * pr.K;
+                    for (int h = 0; h < 2 * nst; h++, rt.next()) {      // word slots: rows kTH*h ..
                         const int slot = rt.slot;
                         if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
                             break;
-                        uint8_t *dst = smem + T::off_tw + slot * tg.slot_bytes;
-                        mbar_arrive_expect_tx(&B.twfull[slot], sp.bytes);
-                        for (int p = 0; p < T::nproj; p++)
-                            if (sp.on[p])
-                                for (int t = 0; t < T::T; t++)
-                                    bulk_g2s(dst + (p * T::T + t) * tg.row_bytes, row_of(sp, p, s * T::T + t),
-                                             256 * sp.K[p], &B.twfull[slot]);
+                        uint8_t *dst = smem + S::off_tw + slot * tg.slot_bytes;
+                        mbar_arrive_expect_tx(&B.twfull[slot], bytes);
+                        for (int t = 0; t < kTH; t++)
+                            bulk_g2s(dst + t * tg.row_bytes, tr0 + (size_t)(h * kTH + t) * ntn * (8 * pr.K),
+                                     256 * pr.K, &B.twfull[slot]);
                     }
                 }
-                cur = nxt;
-                cit = nit;
             }
         }
     } else if (warp == 1) {
@@ -800,34 +785,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             int bs = 0, cur_geom = 0;                 // B ring slot, geometry (stage bytes)
             // descriptors of A slot 0 / B ring byte 0; offsets are added in
             // 16-byte units to the address field
-            const uint64_t adesc0 = smem_desc(smem_addr(smem + T::off_a), 128, T::SBO);
-            const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + T::off_b), 16 * T::KS, 2 * T::KS);
+            const uint64_t adesc0 = smem_desc(smem_addr(smem + S::off_a), 128, S::SBO);
+            const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + S::off_b), 1024, 128);
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = item_b_geom<MODE>(it.nrows);
+                const BGeom bg = b_geom(it.nrows);
                 if (bg.stage_bytes != cur_geom) {
                     bs = 0;
                     cur_geom = bg.stage_bytes;
                 }
-                const uint32_t bproj16 = bg.proj_bytes >> 4, bstage16 = bg.stage_bytes >> 4;
-                // paired linear items: half h (rows 256h..) is B box h and
-                // TMEM columns 256h..; otherwise one half
-                const int nh = item_halves<MODE>(it.nrows);
-                const int rows0 = min(it.nrows, kNT);
-                const uint32_t idesc = instr_desc(max(16, (rows0 + 15) & ~15));
-                const uint32_t idesc1 = instr_desc(max(16, (max(it.nrows - kNT, 0) + 15) & ~15));
-                if (nit > 0 && !wait_bar(B.accempty, (nit - 1) & 1, abort, a.hdr))
+                const uint32_t bstage16 = bg.stage_bytes >> 4;
+                const uint32_t bsub16 = (uint32_t)(bg.rb * 128) >> 4;   // second box of a stage
+                const uint32_t idesc = instr_desc(max(16, (it.nrows + 15) & ~15));
+                const uint32_t buf = nit & 1, use = nit >> 1;
+                // the epilogue has drained this buffer's previous item
+                if (use > 0 && !wait_bar(&B.tempty[buf], (use - 1) & 1, abort, a.hdr))
                     break;
                 fence_after();
-                // pass 0 (base, every projection) opens each accumulator; the
-                // residual passes add to it
+                const uint32_t dt = tmem + buf * kNT;
+                // pass 0 (base) opens the accumulator; residual passes add to it
+                bool first = true;
                 for (int ps = 0; ps < tc_num_passes<MODE>(a) && !*abort; ps++) {
-                    if (ps > 0 && !pass_active<MODE>(a, it.e, ps))
+                    if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
                         continue;
-                    bool on[T::nproj];
-#pragma unroll
-                    for (int p = 0; p < T::nproj; p++)
-                        on[p] = pass_alpha<MODE>(a, it.e, p, ps) != 0.0f;
                     for (int s = 0; s < nst; s++, ra.next()) {
                         const int slot = ra.slot;
                         if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
@@ -835,32 +815,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                             break;
                         bphase ^= 1u << bs;
                         fence_after();
-                        const uint64_t ad = adesc0 + (uint32_t)(slot * (T::nproj * T::a_bytes >> 4));
+                        const uint64_t ad = adesc0 + (uint32_t)(slot * (S::a_bytes >> 4));
                         const uint64_t bd = bdesc0 + (uint32_t)(bs * bstage16);
 #pragma unroll
-                        for (int p = 0; p < T::nproj; p++) {
-                            if (!on[p])
-                                continue;
-#pragma unroll
-                            for (int ks = 0; ks < T::KS / 16; ks++)
-                                mma_f16(tmem + p * kNT, ad + (uint32_t)(p * (T::a_bytes >> 4) + ks * 16),
-                                        bd + (uint32_t)(p * bproj16 + ks * 2), idesc,
-                                        (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < kKS / 16; ks++) {
+                            const uint32_t boff = (ks >= kKS / 32 ? bsub16 : 0u) + (uint32_t)((ks % (kKS / 32)) * 2);
+                            mma_f16(dt, ad + (uint32_t)(ks * 16), bd + boff, idesc, (first && ks == 0) ? 0u : 1u);
                         }
-                        if (MODE != kModeGateUp && nh == 2 && on[0]) {
-#pragma unroll
-                            for (int ks = 0; ks < T::KS / 16; ks++)
-                                mma_f16(tmem + kNT, ad + (uint32_t)(ks * 16),
-                                        bd + (uint32_t)(bproj16 + ks * 2), idesc1,
-                                        (ps > 0 || s > 0 || ks > 0) ? 1u : 0u);
-                        }
+                        first = false;
                         mma_commit(&B.empty[slot]);
                         mma_commit(&B.bempty[bs]);
                         if (++bs == bg.nslots)
                             bs = 0;
                     }
                 }
-                mma_commit(B.accfull);
+                mma_commit(&B.tfull[buf]);
             }
         }
     } else if (warp == kBWarp) {
@@ -880,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items && !*abort; item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
-                const BGeom bg = item_b_geom<MODE>(it.nrows);
+                const BGeom bg = b_geom(it.nrows);
                 if (bg.stage_bytes != cur_geom) {
                     // slots of the old geometry overlap the new ones: drain the ring
                     for (int j = 0; ok && j < kMaxBSlots; j++)
@@ -889,112 +858,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                     cur_geom = bg.stage_bytes;
                 }
                 const CUtensorMap *map = &maps.act[bg.map];
+                const int x0 = (MODE == kModeGateUp) ? it.p * a.in_f : 0;
                 // the same activation tiles again for every residual pass
                 for (int ps = 0; ok && ps < tc_num_passes<MODE>(a); ps++) {
-                    if (ps > 0 && !pass_active<MODE>(a, it.e, ps))
+                    if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
                         continue;
                     for (int s = 0; ok && s < nst; s++, bs = (bs + 1 == bg.nslots) ? 0 : bs + 1) {
                         if (!(ok = reclaim(bs)))
                             break;
                         pend |= 1u << bs;
-                        uint8_t *dst = smem + T::off_b + bs * bg.stage_bytes;
+                        uint8_t *dst = smem + S::off_b + bs * bg.stage_bytes;
                         mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
-                        for (int p = 0; p < T::nproj; p++)
-                            tma_load_2d(dst + p * bg.proj_bytes, map, p * a.in_f + s * T::KS, it.row0,
-                                        &B.bfull[bs]);
-                        if (item_halves<MODE>(it.nrows) == 2)
-                            tma_load_2d(dst + bg.proj_bytes, map, s * T::KS, it.row0 + kNT, &B.bfull[bs]);
+                        tma_load_2d(dst, map, x0 + s * kKS, it.row0, &B.bfull[bs]);
+                        tma_load_2d(dst + bg.rb * 128, map, x0 + s * kKS + kKS / 2, it.row0, &B.bfull[bs]);
                     }
                 }
             }
             // every load this thread issued is consumed by an MMA before the
             // CTA ends; nothing to wait for here
         }
+    } else if (warp >= kEpiWarp0) {
+        // ---------------- epilogue (warps 19..22): finished buffers, in item order
+        const int ew = warp - kEpiWarp0, q = warp & 3;   // TMEM lane quarter = warp % 4
+        float *zs = reinterpret_cast<float *>(smem + S::off_zs);
+        volatile int *go = reinterpret_cast<volatile int *>(smem + S::off_misc + 24);
+        uint32_t nit = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, nit++) {
+            const TcItem it = tc_item<MODE>(a, item);
+            const uint32_t buf = nit & 1, use = nit >> 1;
+            // one thread waits for the buffer; the four warps learn the
+            // outcome together at the named barrier, so all of them take the
+            // same barriers until the end
+            if (ew == 0 && lane == 0)
+                *go = !*abort && wait_bar(&B.tfull[buf], use & 1, abort, a.hdr);
+            named_barrier(2, kEpiThreads);
+            const bool ok = *go != 0;
+            named_barrier(2, kEpiThreads);
+            if (!ok)
+                break;
+            fence_after();
+            tc_item_epilogue<MODE>(a, it, tmem + buf * kNT, zs, ew, q);
+            fence_before();
+            warp_arrive(&B.tempty[buf]);
+        }
     } else {
-        // ---------------- decode + epilogue (warps 2..17)
+        // ---------------- decode (warps 2..17)
         const int dt = tid - 64;                 // 0..511
-        const int dw = dt >> 5;                  // decode warp 0..15
-        const int p = (MODE == kModeGateUp) ? (dt >> 8) : 0;
-        const int t = (MODE == kModeGateUp) ? ((dt >> 7) & 1) : (dt >> 7);
-        const int m = dt & 127;
-        float *zs = reinterpret_cast<float *>(smem + T::off_zs);
+        const int t = dt >> 7;                   // trellis row of the stage
+        const int m = dt & 127;                  // output of the block
         RingPos<kStages> ra;
         RingPosN rt;
         rt.n = tg.nslots;
-        uint32_t nit = 0;
-        for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
+        for (int item = blockIdx.x; item < n_items && !warp_aborted(abort); item += gridDim.x) {
             const TcItem it = tc_item<MODE>(a, item);
-            if (!tc_item_decode<MODE>(a, smem, B, abort, it, ra, rt, tg, p, t, m) || *abort)
+            if (!tc_item_decode<MODE>(a, smem, B, abort, it, ra, rt, tg, t, m))
                 break;
-            // ---- epilogue: TMEM -> shared (32 routes at a time) -> per-row epilogue
-            if (!wait_bar(B.accfull, nit & 1, abort, a.hdr))
-                break;
-            fence_after();
-            const int q = (warp & 3);                 // TMEM lane quarter of this warp
-            GateUpConsts cg;
-            DownConsts cd;
-            if (MODE == kModeGateUp)
-                epi_gateup_consts(a, it.e, it.nbk, cg);
-            else if (MODE == kModeLinear)
-                epi_linear_consts(a, it.nbk, cd);
-            else
-                epi_down_consts(a, it.e, it.nbk, cd);
-            float fac[2];
-            for (int pp = 0; pp < T::nproj; pp++)
-                fac[pp] = (proj_ref<MODE>(a, it.e, pp).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
-            // the four warps of a lane quarter split the interval's columns
-            const int jq = dw >> 2;
-            for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
-                if (MODE == kModeGateUp) {
-                    const int pp = jq >> 1, half = jq & 1;
-                    uint32_t v[16];
-                    tmem_ld<16>(tmem + ((uint32_t)(32 * q) << 16) + pp * kNT + r0 + half * 16, v);
-#pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        zs[(pp * kEpiRows + half * 16 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[pp];
-                } else {
-                    uint32_t v[8];
-                    tmem_ld<8>(tmem + ((uint32_t)(32 * q) << 16) + r0 + jq * 8, v);
-#pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        zs[(jq * 8 + j) * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac[0];
-                }
-                named_barrier(1, kDecThreads);
-                // rows r0 + dw and r0 + dw + 16 of this warp
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int rr = dw + 16 * h, r = r0 + rr;
-                    if (r < it.nrows) {
-                        if (MODE == kModeGateUp) {
-                            float gv[4], uv[4];
-#pragma unroll
-                            for (int i = 0; i < 4; i++) {
-                                gv[i] = zs[rr * kZsLd + 4 * lane + i];
-                                uv[i] = zs[(kEpiRows + rr) * kZsLd + 4 * lane + i];
-                            }
-                            epi_gateup_row(a, cg, it.nbk, it.row0 + r, gv, uv);
-                        } else {
-                            float z[4];
-#pragma unroll
-                            for (int i = 0; i < 4; i++)
-                                z[i] = zs[rr * kZsLd + 4 * lane + i];
-                            if (MODE == kModeLinear)
-                                epi_linear_row(a, cd, it.nbk, it.row0 + r, z);
-                            else
-                                epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
-                        }
-                    }
-                }
-                named_barrier(1, kDecThreads);
-            }
-            fence_before();
-            warp_arrive(B.accempty);
-            if (MODE == kModeDown) {
-                // all of this item's staged rows, then one fence, then the counters
-                __threadfence();
-                named_barrier(1, kDecThreads);
-                epi_down_combine_rows(a, it.nbk, it.row0, it.nrows, dw, kDecWarps);
-            }
         }
     }
 
@@ -1012,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     if (warp == 1) {
         fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     ::"r"(tmem), "r"(T::tmem_cols) : "memory");
+                     ::"r"(tmem), "r"(Smem::tmem_cols) : "memory");
     }
 }
 
@@ -1022,7 +940,7 @@ cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStrea
     TcMapsDev m;
     static_assert(sizeof(m.act) == sizeof(maps.act), "tensor map table");
     memcpy(m.act, maps.act, sizeof(m.act));
-    k_expert_tc<MODE><<<grid, kThreads, Traits<MODE>::total, s>>>(a, m);
+    k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
     return cudaGetLastError();
 }
 
@@ -1030,7 +948,7 @@ template <int MODE>
 cudaError_t set_attr_tc()
 {
     cudaError_t e = cudaFuncSetAttribute(k_expert_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Traits<MODE>::total);
+                                         Smem::total);
     if (e != cudaSuccess)
         return e;
     return cudaFuncSetAttribute(k_expert_tc<MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -23,8 +23,6 @@ struct RoutePackArgs {
     // 1700).  A layer whose residual stages all have scale zero is the plain
     // forward, so the model never depends on the stages.
     int tc_rows, cost_rg, dec_unit_cost;
-    // prefill regime: the down kernel's items are the capacity tiles
-    int down_tiles;
     int32_t *offsets, *packed, *tiles, *info;
     int32_t *zero;                  // words to clear (per-call counters), or null
     int nzero;
@@ -64,9 +62,8 @@ struct GemmArgs {
     int in_f, out_f, nb, nchunks;
     int32_t *hdr;
     const void *rg;                 // int4 row groups (fused layer)
-    // linear: host-planned work; lin_pair: tcgen05 items of two 256-row
-    // halves sharing each decoded weight tile (two MMAs into 512 TMEM columns)
-    int M, n_items_host, split_host, lin_pair;
+    // linear: host-planned work
+    int M, n_items_host, split_host;
     const uint16_t *act;            // fp16 rows (rotated activations)
     long act_row_stride;            // halves between rows
     // gate/up of small decode-regime layers: rotate the raw activations x
@@ -89,13 +86,11 @@ struct GemmArgs {
     // split partials
     float *part;
     int32_t *cnt_split;
-    // prefill-regime down items are the capacity tiles (<= 512 routes, one or
-    // two 256-route halves) instead of the row groups
-    const int32_t *tiles;
-    int down_tiles;
     // outputs
     uint16_t *ad;                   // gate/up: fp16 [R][inter]
-    float *stage;                   // down: fp32 [R][hidden]
+    // fp32 staging: down [R][hidden] (flat route order); prefill-regime
+    // gate/up [R][2][inter] (packed order: rotated gate, rotated up)
+    float *stage;
     const int32_t *packed;
     int topk;
     const void *rw;
@@ -113,18 +108,21 @@ cudaError_t launch_gemm_gateup(bool additive, int nrb, const GemmArgs &a, int gr
 cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
 // Prefill-regime activation tensor maps: 2D fp16 [rows][cols] views of the
-// rotated activations, one map per box height 16 << i rows; a box {KS, 16 << i}
-// (swizzled: 64-byte rows for KS = 32, 128-byte rows for KS = 64) is one
-// stage's B tile of one projection.  Inputs per stage: gate/up 32, down 64.
+// rotated activations, one map per box height 16 << i rows; a box {kTcKs,
+// 16 << i} (128-byte rows, 128-byte swizzle) is one stage's B tile.
 constexpr int kTcMaps = 5;
-constexpr int kTcKsGateUp = 32;
-constexpr int kTcKsDown = 64;
+constexpr int kTcKs = 64;
 struct TcMaps {
     CUtensorMap act[kTcMaps];
 };
 cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t launch_tc_linear(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
+// Prefill-regime layer steps between and after the GEMMs (no-ops unless the
+// route-pack plan chose that regime): SwiGLU + down-input rotation of the
+// staged gate/up rows, and the route-weighted combine of the staged down rows.
+cudaError_t launch_tc_gu_finish(const GemmArgs &a, int sms, cudaStream_t s);
+cudaError_t launch_tc_combine(const GemmArgs &a, int sms, cudaStream_t s);
 cudaError_t tc_set_attributes();
 int tc_rows_per_item();
 cudaError_t gemm_gateup_set_attributes();

@@ -72,7 +72,10 @@ EXL3_HD inline MoeLayout moe_layout(int M, int topk, int E, int hidden, int inte
     L.rg = o;       o = align_up(o + (size_t)L.max_rg * 16, 256);
     L.arot = o;     o = align_up(o + (size_t)L.R * 2 * hidden * 2, 256);
     L.ad = o;       o = align_up(o + (size_t)L.R * inter * 2, 256);
-    L.stage = o;    o = align_up(o + (size_t)L.R * hidden * 4, 256);
+    // fp32 staging: the down rows [R][hidden]; above 128 tokens also the
+    // prefill regime's rotated gate and up rows [R][2][inter]
+    const size_t stage_w = (M > 128 && 2 * inter > hidden) ? 2 * (size_t)inter : (size_t)hidden;
+    L.stage = o;    o = align_up(o + (size_t)L.R * stage_w * 4, 256);
     // counters (cleared by every call): combine, gate/up split, down split
     L.cnt = o;      o += (size_t)M * L.nb2 * 4;
     L.cnt1 = o;     o += (size_t)L.split_pairs1 * 4;

@@ -80,8 +80,9 @@ __device__ void write_plan_header(const RoutePackArgs &a, int ntiles, int nact, 
     const int split2 = !use_tc && a.nchunks2 > 1 && pairs2 <= min(lim, a.split_pairs2);
     a.info[kHdrSplit1] = split1;
     a.info[kHdrSplit2] = split2;
-    a.info[kHdrNItems1] = split1 ? pairs1 * a.nchunks1 : pairs1;
-    a.info[kHdrNItems2] = (use_tc && a.down_tiles) ? ntiles * a.nb2 : (split2 ? pairs2 * a.nchunks2 : pairs2);
+    // prefill-regime gate/up items are single projections: two per pair
+    a.info[kHdrNItems1] = use_tc ? 2 * pairs1 : (split1 ? pairs1 * a.nchunks1 : pairs1);
+    a.info[kHdrNItems2] = split2 ? pairs2 * a.nchunks2 : pairs2;
     a.info[kHdrRegime] = use_tc ? 1 : 0;
 }
 
