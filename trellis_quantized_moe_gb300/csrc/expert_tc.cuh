@@ -17,7 +17,7 @@
 // barrier wait, tcgen05.commit and activation copy then serves 8 MMAs (the
 // single issuing thread's own instruction latencies, not the tensor pipe,
 // bound 64-input stages).  Roles:
-//   warp 0      lane 0 streams trellis rows with cp.async.bulk into a 24 KB
+//   warp 0      streams trellis rows with cp.async.bulk (lane t: row t) into a 24 KB
 //               ring of word slots (4 rows each, two per stage) sized by the
 //               layer's largest K, mbarrier complete_tx, running into the
 //               next item as slots free up;
@@ -30,9 +30,9 @@
 //               weights each (the two halves of the mcg/3inst word summed in
 //               fp16, mul1 as the exact integer byte sum - 510) and stores
 //               them, 16 bytes at a time, into a K-major no-swizzle A tile;
-//   warp 18     lane 0 loads the activation (B) tiles with 2D TMA, two boxes
-//               per stage, into a byte ring that runs as far ahead of the
-//               MMAs as it has room;
+//   warp 18     loads the activation (B) tiles with 2D TMA, two boxes per
+//               stage (lanes 0 and 1), into a byte ring that runs as far
+//               ahead of the MMAs as it has room;
 //   warps 19-22 epilogue: read the finished buffer (tcgen05.ld, one TMEM lane
 //               quarter each), transpose 16 routes at a time through shared
 //               memory and run the per-row output rotation: gate/up write
@@ -84,7 +84,8 @@ struct Smem {
     static constexpr int off_b = off_a + kStages * a_bytes;
     static constexpr int off_tw = off_b + kBRingBytes;
     static constexpr int off_zs = off_tw + kTwRingBytes;        // epilogue transpose, 16 routes
-    static constexpr int off_bar = off_zs + kEpiRows * kZsLd * 4;
+    static constexpr int off_rows = off_zs + kEpiRows * kZsLd * 4;   // down: staging row of each item row
+    static constexpr int off_bar = off_rows + kNT * 4;
     static constexpr int nbar = 2 * kStages + 2 * kTwSlots + 2 * kMaxBSlots + 4;
     static constexpr int off_misc = off_bar + nbar * 8;
     static constexpr int total = off_misc + 64;
@@ -101,13 +102,12 @@ struct TcMapsDev {
     CUtensorMap act[kTcMaps];
 };
 
-// Activation ring geometry of one work item: RB = the item's routes rounded
-// up to a power of two (>= 16), one stage = one box of RB rows; as many stages
-// as fit in the ring (at most 16).  Items of the same geometry continue one
-// ring; a change of geometry first drains it.  (Rounding to a power of two
-// fetches about 5% more rows than rounding to 16 on a Zipf-routed layer.)
+// Activation geometry of one work item: RB = the item's routes rounded up to
+// a power of two (>= 16); a stage is two TMA boxes of RB rows x 128 bytes.
+// (Rounding to a power of two fetches about 5% more rows than rounding to 16
+// on a Zipf-routed layer.)
 struct BGeom {
-    int rb, map, stage_bytes, nslots;
+    int rb, map, stage_bytes;
 };
 
 __device__ __forceinline__ BGeom b_geom(int nrows)
@@ -117,10 +117,27 @@ __device__ __forceinline__ BGeom b_geom(int nrows)
     while ((16 << g.map) < nrows)
         g.map++;
     g.rb = 16 << g.map;
-    g.stage_bytes = g.rb * kKS * 2;          // two boxes of rb rows x 128 bytes
-    g.nslots = min(kMaxBSlots, kBRingBytes / g.stage_bytes);
+    g.stage_bytes = g.rb * kKS * 2;
     return g;
 }
+
+// Placement of activation stages in the B byte ring: stages of any geometry
+// follow each other, each at the first offset after the previous one that
+// leaves room for it (else at 0); at most kMaxBSlots are in flight, stage i
+// signalling barrier i % kMaxBSlots.  The producer and the MMA thread replay
+// the same sequence of sizes, so they agree on every offset without
+// exchanging them, and items of different sizes never drain the ring.
+struct BRing {
+    uint32_t head = 0;      // next free byte
+    uint32_t n = 0;         // stages placed
+    __device__ __forceinline__ uint32_t place(uint32_t bytes)
+    {
+        const uint32_t o = head + bytes > (uint32_t)kBRingBytes ? 0u : head;
+        head = o + bytes;
+        n++;
+        return o;
+    }
+};
 
 // Bounded mbarrier wait shared by every role: gives up after ~2^31 cycles or
 // as soon as another thread has given up, and then reports false.
@@ -211,6 +228,18 @@ __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t ad, uint64_t bd
                  ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate));
 }
 
+// The same with the descriptors given as 32-bit halves: the address fields
+// of a stage's eight MMAs differ by small constants, so the issuing thread
+// adds to the low words only (fewer instructions in the single-thread loop).
+__device__ __forceinline__ void mma_f16_lo(uint32_t dtmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                           uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n .reg .pred p;\n .reg .b64 ad, bd;\n mov.b64 ad, {%1, %2};\n mov.b64 bd, {%3, %4};\n"
+                 " setp.ne.b32 p, %6, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n"
+                 ::"r"(dtmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -241,6 +270,25 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[NREG])
                      : "r"(taddr));
     }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// tcgen05.ld of 16 columns without the wait, and the wait that completes it:
+// the wait names the destination registers as in/out operands, so no use of
+// them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+                 :: "memory");
 }
 
 __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b)
@@ -302,22 +350,30 @@ struct ColumnStates<K, 16> {
 // The 16 states of the window -> 16 fp16 weights in k order (8 half2 words):
 // mcg/3inst sum their two fp16 halves in fp16 (one rounding), mul1 gives the
 // exact integer byte sum - 510.
-template <int K, int CB>
-__device__ __forceinline__ void decode_column(const uint32_t *tile, const ColumnWindow<K> &cw,
-                                              const HashConsts &hc, uint32_t w[8])
+// The window of the column's 16 states as normalised words X (bit 0 of state
+// 0 at the top of X[0]): the shared-memory reads of a column run.  Once X is
+// in registers the word slot may be refilled.
+template <int K>
+__device__ __forceinline__ void column_bits(const uint32_t *tile, const ColumnWindow<K> &cw,
+                                            uint32_t (&X)[ColumnWindow<K>::NX + 1])
 {
     constexpr int NX = ColumnWindow<K>::NX;
-    constexpr uint32_t A = CB == EXL3_CB_MUL1 ? 0x83DCD12Du : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
-    constexpr uint32_t B = CB == EXL3_CB_3INST ? 64248484u : 0u;
     uint32_t W[NX + 1];
 #pragma unroll
     for (int j = 0; j <= NX; j++)
         W[j] = tile[cw.idx[j]];
-    uint32_t X[NX + 1];
 #pragma unroll
     for (int j = 0; j < NX; j++)
         X[j] = __funnelshift_l(W[j + 1], W[j], cw.o);
     X[NX] = 0;
+}
+
+template <int K, int CB>
+__device__ __forceinline__ void decode_bits(const uint32_t (&X)[ColumnWindow<K>::NX + 1], const HashConsts &hc,
+                                            uint32_t w[8])
+{
+    constexpr uint32_t A = CB == EXL3_CB_MUL1 ? 0x83DCD12Du : (CB == EXL3_CB_3INST ? 89226354u : 0xCBAC1FEDu);
+    constexpr uint32_t B = CB == EXL3_CB_3INST ? 64248484u : 0u;
     uint32_t x[16];
     uint32_t st[16];
     ColumnStates<K, 0>::run(X, st);
@@ -509,11 +565,15 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
         if (!warp_wait_bar(&B.twfull[rt.slot], rt.phase, abort, a.hdr) ||
             !warp_wait_bar(&B.twfull[rt1.slot], rt1.phase, abort, a.hdr))
             return false;
+        uint32_t X0[ColumnWindow<K>::NX + 1], X1[ColumnWindow<K>::NX + 1];
+        column_bits<K>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt.slot * tg.slot_bytes + tile_off), cw, X0);
+        column_bits<K>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt1.slot * tg.slot_bytes + tile_off), cw, X1);
+        // the words are in registers (X depends on them): the slots can be refilled
+        warp_arrive(&B.twempty[rt.slot]);
+        warp_arrive(&B.twempty[rt1.slot]);
         uint32_t w0[8], w1[8];
-        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt.slot * tg.slot_bytes + tile_off),
-                             cw, hc, w0);
-        decode_column<K, CB>(reinterpret_cast<const uint32_t *>(smem + S::off_tw + rt1.slot * tg.slot_bytes + tile_off),
-                             cw, hc, w1);
+        decode_bits<K, CB>(X0, hc, w0);
+        decode_bits<K, CB>(X1, hc, w1);
         if (RES) {
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -521,8 +581,6 @@ __device__ __forceinline__ bool tc_stages(const GemmArgs &a, uint8_t *smem, cons
                 w1[i] = hmul2_u32(w1[i], alpha2);
             }
         }
-        warp_arrive(&B.twempty[rt.slot]);
-        warp_arrive(&B.twempty[rt1.slot]);
         // an A slot is free once the MMAs of its previous stage completed; the
         // decode above does not need it
         if (!warp_wait_bar(&B.empty[ra.slot], ra.phase ^ 1, abort, a.hdr))
@@ -626,10 +684,12 @@ __device__ __forceinline__ void epi_gu_half_row(const GemmArgs &a, const DownCon
 // The epilogue warps' share of one item: buffer `buf` of TMEM -> 16 routes at
 // a time through shared memory -> per-row output rotation.  Warp ew (0..3)
 // reads TMEM lane quarter q = its warp index % 4 and runs routes ew*4..ew*4+3
-// of each interval.
+// of each interval.  The next interval's tcgen05.ld is in flight while the
+// current one is processed; down items look their staging rows up once per
+// item (a dependent global load per row would stall every interval).
 template <int MODE>
 __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem &it, uint32_t tbuf, float *zs,
-                                                 int ew, int q)
+                                                 int *rowmap, int ew, int q)
 {
     const int lane = threadIdx.x & 31;
     DownConsts cd;
@@ -641,14 +701,21 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
         load_half4(reinterpret_cast<const uint16_t *>(a.t_svh[it.e * 3 + pi]), col, cd.sv);
         load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[it.e * 3 + pi]), col, cd.sc);
     }
+    if (MODE == kModeDown)
+        for (int r = ew * 32 + lane; r < it.nrows; r += kEpiThreads)
+            rowmap[r] = a.packed[it.row0 + r];
     const float fac = (proj_ref<MODE>(a, it.e, it.p).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
+    const uint32_t taddr = tbuf + ((uint32_t)(32 * q) << 16);
+    uint32_t v[16];
+    tmem_ld16_issue(taddr, v);
     for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
-        uint32_t v[16];
-        tmem_ld<16>(tbuf + ((uint32_t)(32 * q) << 16) + r0, v);
+        tmem_ld16_wait(v);
 #pragma unroll
         for (int j = 0; j < 16; j++)
             zs[j * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac;
         named_barrier(2, kEpiThreads);
+        if (r0 + kEpiRows < it.nrows)
+            tmem_ld16_issue(taddr + r0 + kEpiRows, v);
 #pragma unroll
         for (int h = 0; h < 4; h++) {
             const int rr = 4 * ew + h, r = r0 + rr;
@@ -657,12 +724,18 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
 #pragma unroll
                 for (int i = 0; i < 4; i++)
                     z[i] = zs[rr * kZsLd + 4 * lane + i];
-                if (MODE == kModeGateUp)
+                if (MODE == kModeGateUp) {
                     epi_gu_half_row(a, cd, it.p, it.nbk, it.row0 + r, z);
-                else if (MODE == kModeLinear)
+                } else if (MODE == kModeLinear) {
                     epi_linear_row(a, cd, it.nbk, it.row0 + r, z);
-                else
-                    epi_down_stage_row(a, cd, it.nbk, it.row0 + r, z);
+                } else {
+                    warp_hadamard128(z);
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        z[i] = z[i] * kInvSqrt128 * cd.sv[i] * cd.sc[i];
+                    *reinterpret_cast<float4 *>(a.stage + (size_t)rowmap[r] * a.out_f + it.nbk * kHb + 4 * lane) =
+                        make_float4(z[0], z[1], z[2], z[3]);
+                }
             }
         }
         named_barrier(2, kEpiThreads);
@@ -751,29 +824,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
     const TwGeom tg = tw_geom(*kmax_slot);
 
     if (warp == 0) {
-        // ---------------- producer: trellis rows -> word slots
-        if (lane == 0) {
-            RingPosN rt;
-            rt.n = tg.nslots;
-            const int npass = tc_num_passes<MODE>(a);
-            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-                const TcItem it = tc_item<MODE>(a, item);
-                for (int ps = 0; ps < npass && !*abort; ps++) {
-                    if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
-                        continue;
-                    const ProjRef pr = pass_ref<MODE>(a, it.e, it.p, ps);
-                    const uint32_t *tr0 = pr.trellis + (size_t)it.nbk * 8 * (8 * pr.K);
-                    const uint32_t bytes = kTH * 256 * pr.K;
-                    for (int h = 0; h < 2 * nst; h++, rt.next()) {      // word slots: rows kTH*h ..
-                        const int slot = rt.slot;
-                        if (!wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr))
-                            break;
-                        uint8_t *dst = smem + S::off_tw + slot * tg.slot_bytes;
+        // ---------------- producer: trellis rows -> word slots (the whole warp
+        // runs the loop; lanes 0..3 each issue one row's bulk copy, so a slot
+        // costs one copy instruction issue)
+        RingPosN rt;
+        rt.n = tg.nslots;
+        const int npass = tc_num_passes<MODE>(a);
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items && !warp_aborted(abort); item += gridDim.x) {
+            const TcItem it = tc_item<MODE>(a, item);
+            for (int ps = 0; ok && ps < npass; ps++) {
+                if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
+                    continue;
+                const ProjRef pr = pass_ref<MODE>(a, it.e, it.p, ps);
+                const uint32_t *tr0 = pr.trellis + (size_t)it.nbk * 8 * (8 * pr.K);
+                const uint32_t bytes = kTH * 256 * pr.K;
+                for (int h = 0; h < 2 * nst; h++, rt.next()) {      // word slots: rows kTH*h ..
+                    const int slot = rt.slot;
+                    if (!(ok = warp_wait_bar(&B.twempty[slot], rt.phase ^ 1, abort, a.hdr)))
+                        break;
+                    uint8_t *dst = smem + S::off_tw + slot * tg.slot_bytes;
+                    if (lane == 0)
                         mbar_arrive_expect_tx(&B.twfull[slot], bytes);
-                        for (int t = 0; t < kTH; t++)
-                            bulk_g2s(dst + t * tg.row_bytes, tr0 + (size_t)(h * kTH + t) * ntn * (8 * pr.K),
-                                     256 * pr.K, &B.twfull[slot]);
-                    }
+                    __syncwarp();
+                    if (lane < kTH)
+                        bulk_g2s(dst + lane * tg.row_bytes, tr0 + (size_t)(h * kTH + lane) * ntn * (8 * pr.K),
+                                 256 * pr.K, &B.twfull[slot]);
                 }
             }
         }
@@ -781,20 +857,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         // ---------------- MMA issuer
         if (lane == 0) {
             RingPos<kStages> ra;
-            uint32_t nit = 0, bphase = 0;            // bphase: parity bit per B slot
-            int bs = 0, cur_geom = 0;                 // B ring slot, geometry (stage bytes)
+            uint32_t nit = 0, bphase = 0;            // bphase: parity bit per B stage barrier
+            BRing br;
             // descriptors of A slot 0 / B ring byte 0; offsets are added in
             // 16-byte units to the address field
             const uint64_t adesc0 = smem_desc(smem_addr(smem + S::off_a), 128, S::SBO);
             const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + S::off_b), 1024, 128);
+            const uint32_t adlo = (uint32_t)adesc0, adhi = (uint32_t)(adesc0 >> 32);
+            const uint32_t bdlo = (uint32_t)bdesc0, bdhi = (uint32_t)(bdesc0 >> 32);
             for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
                 const TcItem it = tc_item<MODE>(a, item);
                 const BGeom bg = b_geom(it.nrows);
-                if (bg.stage_bytes != cur_geom) {
-                    bs = 0;
-                    cur_geom = bg.stage_bytes;
-                }
-                const uint32_t bstage16 = bg.stage_bytes >> 4;
                 const uint32_t bsub16 = (uint32_t)(bg.rb * 128) >> 4;   // second box of a stage
                 const uint32_t idesc = instr_desc(max(16, (it.nrows + 15) & ~15));
                 const uint32_t buf = nit & 1, use = nit >> 1;
@@ -810,23 +883,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                         continue;
                     for (int s = 0; s < nst; s++, ra.next()) {
                         const int slot = ra.slot;
+                        const int bs = (int)(br.n % kMaxBSlots);
+                        const uint32_t boff = br.place((uint32_t)bg.stage_bytes);
                         if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
                             !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
                             break;
                         bphase ^= 1u << bs;
                         fence_after();
-                        const uint64_t ad = adesc0 + (uint32_t)(slot * (S::a_bytes >> 4));
-                        const uint64_t bd = bdesc0 + (uint32_t)(bs * bstage16);
+                        // address fields stay below 2^14 (shared memory < 256 KB): 32-bit adds
+                        const uint32_t alo = adlo + (uint32_t)(slot * (S::a_bytes >> 4));
+                        const uint32_t blo = bdlo + (boff >> 4);
+                        const uint32_t blo2 = blo + bsub16;
+                        mma_f16_lo(dt, alo, adhi, blo, bdhi, idesc, first ? 0u : 1u);
 #pragma unroll
-                        for (int ks = 0; ks < kKS / 16; ks++) {
-                            const uint32_t boff = (ks >= kKS / 32 ? bsub16 : 0u) + (uint32_t)((ks % (kKS / 32)) * 2);
-                            mma_f16(dt, ad + (uint32_t)(ks * 16), bd + boff, idesc, (first && ks == 0) ? 0u : 1u);
-                        }
+                        for (int ks = 1; ks < kKS / 16; ks++)
+                            mma_f16_lo(dt, alo + (uint32_t)(ks * 16), adhi,
+                                       (ks >= kKS / 32 ? blo2 : blo) + (uint32_t)((ks % (kKS / 32)) * 2), bdhi, idesc,
+                                       1u);
                         first = false;
                         mma_commit(&B.empty[slot]);
                         mma_commit(&B.bempty[bs]);
-                        if (++bs == bg.nslots)
-                            bs = 0;
                     }
                 }
                 mma_commit(&B.tfull[buf]);
@@ -834,53 +910,68 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         }
     } else if (warp == kBWarp) {
         // ---------------- activation producer: 2D TMA boxes into the B ring
-        if (lane == 0) {
-            uint32_t pend = 0, ph = 0;                // per B slot: use in flight, parity
-            int bs = 0, cur_geom = 0;
-            auto reclaim = [&](int bs) -> bool {
-                if ((pend >> bs) & 1) {
-                    if (!wait_bar(&B.bempty[bs], (ph >> bs) & 1, abort, a.hdr))
-                        return false;
-                    ph ^= 1u << bs;
-                    pend &= ~(1u << bs);
-                }
-                return true;
-            };
+        // (the whole warp runs the loop; lanes 0 and 1 issue a stage's boxes;
+        // lane j < kMaxBSlots tracks the bytes of in-flight stage barrier j)
+        {
+            uint32_t ph = 0;                          // bempty parity bit per stage barrier
+            uint32_t my_off = 0, my_end = 0;          // lane j: bytes of the stage on barrier j
+            bool my_busy = false;
+            uint32_t tail = 0;                        // oldest stage in flight
+            BRing br;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items && !*abort; item += gridDim.x) {
+            for (int item = blockIdx.x; ok && item < n_items && !warp_aborted(abort); item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
                 const BGeom bg = b_geom(it.nrows);
-                if (bg.stage_bytes != cur_geom) {
-                    // slots of the old geometry overlap the new ones: drain the ring
-                    for (int j = 0; ok && j < kMaxBSlots; j++)
-                        ok = reclaim(j);
-                    bs = 0;
-                    cur_geom = bg.stage_bytes;
-                }
                 const CUtensorMap *map = &maps.act[bg.map];
                 const int x0 = (MODE == kModeGateUp) ? it.p * a.in_f : 0;
                 // the same activation tiles again for every residual pass
                 for (int ps = 0; ok && ps < tc_num_passes<MODE>(a); ps++) {
                     if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
                         continue;
-                    for (int s = 0; ok && s < nst; s++, bs = (bs + 1 == bg.nslots) ? 0 : bs + 1) {
-                        if (!(ok = reclaim(bs)))
+                    for (int s = 0; ok && s < nst; s++) {
+                        const int bs = (int)(br.n % kMaxBSlots);
+                        const uint32_t o = br.place((uint32_t)bg.stage_bytes);
+                        const uint32_t e = o + (uint32_t)bg.stage_bytes;
+                        // retire the oldest stages until none in flight overlaps [o, e)
+                        // and barrier bs is free
+                        while (ok) {
+                            const bool clash = my_busy && my_off < e && o < my_end;
+                            const bool full = br.n - 1 - tail >= (uint32_t)kMaxBSlots;
+                            if (!__any_sync(0xffffffffu, clash) && !full)
+                                break;
+                            const int ts = (int)(tail % kMaxBSlots);
+                            if (!(ok = warp_wait_bar(&B.bempty[ts], (ph >> ts) & 1, abort, a.hdr)))
+                                break;
+                            ph ^= 1u << ts;
+                            if (lane == ts)
+                                my_busy = false;
+                            tail++;
+                        }
+                        if (!ok)
                             break;
-                        pend |= 1u << bs;
-                        uint8_t *dst = smem + S::off_b + bs * bg.stage_bytes;
-                        mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
-                        tma_load_2d(dst, map, x0 + s * kKS, it.row0, &B.bfull[bs]);
-                        tma_load_2d(dst + bg.rb * 128, map, x0 + s * kKS + kKS / 2, it.row0, &B.bfull[bs]);
+                        if (lane == bs) {
+                            my_off = o;
+                            my_end = e;
+                            my_busy = true;
+                        }
+                        uint8_t *dst = smem + S::off_b + o;
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
+                        __syncwarp();
+                        if (lane < 2)
+                            tma_load_2d(dst + lane * bg.rb * 128, map, x0 + s * kKS + lane * (kKS / 2), it.row0,
+                                        &B.bfull[bs]);
                     }
                 }
             }
-            // every load this thread issued is consumed by an MMA before the
+            // every load this warp issued is consumed by an MMA before the
             // CTA ends; nothing to wait for here
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue (warps 19..22): finished buffers, in item order
         const int ew = warp - kEpiWarp0, q = warp & 3;   // TMEM lane quarter = warp % 4
         float *zs = reinterpret_cast<float *>(smem + S::off_zs);
+        int *rowmap = reinterpret_cast<int *>(smem + S::off_rows);
         volatile int *go = reinterpret_cast<volatile int *>(smem + S::off_misc + 24);
         uint32_t nit = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, nit++) {
@@ -897,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             if (!ok)
                 break;
             fence_after();
-            tc_item_epilogue<MODE>(a, it, tmem + buf * kNT, zs, ew, q);
+            tc_item_epilogue<MODE>(a, it, tmem + buf * kNT, zs, rowmap, ew, q);
             fence_before();
             warp_arrive(&B.tempty[buf]);
         }
