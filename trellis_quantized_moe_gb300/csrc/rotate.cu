@@ -21,8 +21,7 @@ __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
         a.hdr_reset[kHdrError] = 0;
     if (a.hdr && a.hdr[kHdrError])
         return;
-    // warp = (RPW consecutive rows, projection, group of 8 128-blocks): packed rows come in runs of one expert, so suh is loaded
-    // once per run and reused for the warp's following rows
+    // warp = (RPW consecutive rows, projection, group of 8 128-blocks)
     const int nblk = a.width / kHb;
     const int ngroups = (nblk + kBlocksPerWarp - 1) / kBlocksPerWarp;
     const long wg = (long)blockIdx.x * 8 + (tid >> 5);
@@ -31,44 +30,82 @@ __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
     const int row0 = (int)(wg / ((long)ngroups * a.nproj)) * RPW;
     if (row0 >= a.rows)
         return;
+    const int nr = min(RPW, a.rows - row0);
     const int blk = grp * kBlocksPerWarp + (lane >> 2);
     const int c = lane & 3;                      // quarter of the block
     const bool active = blk < nblk;              // uniform within each group of 4 lanes
     const int col = (active ? blk : 0) * kHb + kFeat * c;
-    const uint16_t *cur_suh = nullptr;
-    float s[kFeat];
-#pragma unroll 1
-    for (int row = row0; row < row0 + RPW && row < a.rows; row++) {
-        long token;
-        const uint16_t *suh;
+    // the rows' tokens and suh vectors, looked up once, lane i for row i:
+    // the dependent loads of all rows are in flight together
+    long long tok_l = 0;
+    unsigned long long suh_l = 0;
+    if (lane < nr) {
+        const int row = row0 + lane;
         if (a.packed) {
             const int f = a.packed[row];
-            token = f / a.topk;
-            const long long e = a.ids_dtype == EXL3_I64
-                                    ? static_cast<const int64_t *>(a.ids)[f]
-                                    : static_cast<const int32_t *>(a.ids)[f];
-            suh = reinterpret_cast<const uint16_t *>(a.t_suh[e * 3 + p]);
+            tok_l = f / a.topk;
+            const long long e = a.ids_dtype == EXL3_I64 ? static_cast<const int64_t *>(a.ids)[f]
+                                                        : static_cast<const int32_t *>(a.ids)[f];
+            suh_l = static_cast<unsigned long long>(a.t_suh[e * 3 + p]);
         } else {
-            token = row;
-            suh = a.suh;
+            tok_l = row;
+            suh_l = reinterpret_cast<unsigned long long>(a.suh);
         }
-        if (suh != cur_suh) {                    // warp-uniform: depends on the row only
-            load_half32(suh, col, s);
+    }
+    // the next row's activations load while this row is rotated
+    auto load_row = [&](int i, uint4 (&r)[4]) {
+        const long long tok = __shfl_sync(0xffffffffu, tok_l, i);
+        const uint4 *q = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.x) + tok * a.width + col);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            r[k] = q[k];
+    };
+    uint4 cur[4], nxt[4];
+    load_row(0, cur);
+    unsigned long long cur_suh = 0;
+    uint32_t sh[kFeat / 2];                      // suh as fp16 pairs (fewer live registers)
+#pragma unroll 1
+    for (int i = 0; i < nr; i++) {
+        if (i + 1 < nr)
+            load_row(i + 1, nxt);
+        const unsigned long long suh = __shfl_sync(0xffffffffu, suh_l, i);
+        if (suh != cur_suh) {                    // warp-uniform
+            const uint2 *q = reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(suh) + col);
+#pragma unroll
+            for (int k = 0; k < kFeat / 4; k++) {
+                const uint2 r = q[k];
+                sh[2 * k] = r.x;
+                sh[2 * k + 1] = r.y;
+            }
             cur_suh = suh;
         }
         float v[kFeat];
-        load_act32(a.x, (size_t)token * a.width + col, a.act_dtype, v);
 #pragma unroll
-        for (int i = 0; i < kFeat; i++)
-            v[i] *= s[i];
+        for (int k = 0; k < 4; k++) {
+            const uint32_t w[4] = {cur[k].x, cur[k].y, cur[k].z, cur[k].w};
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                float2 f;
+                if (a.act_dtype == EXL3_BF16)
+                    f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[h]));
+                else
+                    f = __half22float2(*reinterpret_cast<const __half2 *>(&w[h]));
+                const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sh[4 * k + h]));
+                v[8 * k + 2 * h] = f.x * sf.x;
+                v[8 * k + 2 * h + 1] = f.y * sf.y;
+            }
+        }
         uint4 out[4];
         rotate_block32(v, c, out);
         if (active) {
-            uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)row * a.nproj + p) * a.width + col);
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(row0 + i) * a.nproj + p) * a.width + col);
 #pragma unroll
             for (int k = 0; k < 4; k++)
                 dst[k] = out[k];
         }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            cur[k] = nxt[k];
     }
 }
 
