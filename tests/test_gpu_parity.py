@@ -407,6 +407,81 @@ def test_three_residual_stages_of_mixed_widths(M):
     assert np.array_equal(a, b)
 
 
+def _dense_moe(w, get_dense, tokens):
+    """Float64 layer from dense per-(expert, projection) weights W[in, out]:
+    the oracle's routing, rotations, SwiGLU and j-ordered combine."""
+    s = w.spec
+    x = act_to_f64(w.x, s.act)
+    from workloads import rw_to_f64
+    rw = rw_to_f64(w.rw, s.rw_dtype)
+    out = np.zeros((len(tokens), s.hidden))
+    for i, t in enumerate(tokens):
+        for j in range(s.topk):
+            e = int(w.ids[t, j])
+            pr = [w.projection(e, q, cache=True) for q in range(3)]
+            g = O.linear_from_dense(x[t:t + 1], get_dense(e, 0), pr[0].suh, pr[0].svh, pr[0].scale)
+            u = O.linear_from_dense(x[t:t + 1], get_dense(e, 1), pr[1].suh, pr[1].svh, pr[1].scale)
+            d = O.linear_from_dense(O.silu(g) * u, get_dense(e, 2), pr[2].suh, pr[2].svh, pr[2].scale)
+            out[i] += float(rw[t, j]) * d[0]
+    return out
+
+
+def test_prefill_additive_rounding_stays_within_its_bound():
+    # Above 128 tokens a residual stage is one more pass over the base
+    # accumulator with its decoded fp16 weights multiplied by fp16(alpha')
+    # (alpha' = alpha * sqrt(21845) over a mul1 base, whose accumulator is
+    # scaled by 1/sqrt(21845) at the end), i.e. W_res -> fp16(fp16(W_res) *
+    # fp16(alpha')) / c: two extra roundings of 2^-11 each per residual
+    # weight, where the decode regime scales the fp32 partial instead.
+    # (1) the kernel equals that model within the layer tolerance, and (2)
+    # the model's departure from the exact stage sum is at most 2^-8 of the
+    # residual stages' own contribution (4x the 2^-10 per-weight bound).
+    from workloads import MoESpec
+    E = 8
+    spec = MoESpec("stages", 512, 256, E, 2, 300, "f16", "i32", "f32", np.full(E, 4),
+                   np.array([CB_MCG, CB_3INST, CB_MUL1, CB_MCG] * 2), seed=391,
+                   residual_K=[3, 1, 5], residual_zero_frac=0.3)
+    w = MoEWorkload(spec)
+    ex = X.DeviceExperts.from_workload(w)
+    gpu = to_f64(run_layer(w, ex, stages=_stages(w)))
+    assert LAST["regime"] == 1
+    tokens = np.arange(0, 300, 7)
+    f16 = lambda a: np.asarray(a, np.float64).astype(np.float16).astype(np.float64)  # noqa: E731
+    cache = {}
+
+    def dense(e, p, mode):
+        key = (e, p, mode)
+        if key not in cache:
+            pr = w.projection(e, p, cache=True)
+            base = O.decode_projection(pr.trellis, pr.K, pr.codebook)
+            c = np.sqrt(21845.0) if pr.codebook == CB_MUL1 else 1.0
+            W = base if pr.codebook == CB_MUL1 else f16(base)      # the kernel's fp16 weight sums
+            if mode == "base":
+                cache[key] = W
+                return W
+            for st in range(1, spec.num_stages):
+                a = float(w.alpha[st - 1, e, p])
+                if a == 0.0:
+                    continue
+                R = O.decode_projection(w.residual(st, e, p), int(spec.residual_K[st - 1]), O.MCG)
+                if mode == "exact":
+                    W = W + a * R
+                else:
+                    W = W + f16(f16(R) * f16(a * c)) / c
+            cache[key] = W
+        return cache[key]
+
+    model = _dense_moe(w, lambda e, p: dense(e, p, "model"), tokens)
+    exact = _dense_moe(w, lambda e, p: dense(e, p, "exact"), tokens)
+    base = _dense_moe(w, lambda e, p: dense(e, p, "base"), tokens)
+    assert_close_linear(gpu[tokens], model, "f16", "prefill additive vs its rounding model")
+    dev = np.linalg.norm(model - exact)
+    contrib = np.linalg.norm(exact - base)
+    assert contrib > 0.05 * np.linalg.norm(exact), "residual stages too small to test"
+    assert dev <= 2.0 ** -8 * contrib, (dev, contrib)
+    assert np.max(np.abs(model - exact)) <= 2.0 ** -8 * np.max(np.abs(exact - base)) + 1e-6
+
+
 # --------------------------------------------------------------------------- contracts
 def test_host_contract_violation_writes_nothing():
     import ctypes

@@ -287,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
     // prefill regime per item of up to tc_rows rows.  Measured cost per item
     // (hidden 5120, inter 1536, K 3-4; other shapes scale both alike): decode
     // regime 10.5 us (8-row groups) or 17 us (16-row groups), prefill regime
-    // 14.4 + 9.8 * rows / 256 us.  The regime with the smaller total wins; the
+    // 12.0 + 8.1 * rows / 256 us (the earlier 14.4 + 9.8 scaled by the
+    // measured GEMM time of the current prefill kernels on the 3072-token
+    // layer, 2.90 -> 2.39 ms).  The regime with the smaller total wins; the
     // choice depends only on the routing.
     // (integer costs in hundredths, so the sums and the choice are exact)
     // Residual stages add the same decode work to both regimes and are left
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_route_pack(RoutePackArgs a)
             const int len = min(a.capacity, cnt - s * a.capacity);
             cd += (long long)a.dec_unit_cost * ((len + a.cost_rg - 1) / a.cost_rg);
             for (int r = 0; r < len; r += a.tc_rows)
-                ct += 1440 + 980 * min(a.tc_rows, len - r) / 256;
+                ct += 1200 + 810 * min(a.tc_rows, len - r) / 256;
         }
         atomicAdd(reinterpret_cast<unsigned long long *>(&s_cost[0]), (unsigned long long)cd);
         atomicAdd(reinterpret_cast<unsigned long long *>(&s_cost[1]), (unsigned long long)ct);
