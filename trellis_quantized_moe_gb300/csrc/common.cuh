@@ -76,11 +76,13 @@ EXL3_DEV void warp_hadamard128(float v[4])
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = lane & m;
+        // upper lane: o - v, lower lane: v + o, as one fma with a +-1 factor
+        // (exact product, same single rounding)
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
+            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = __fmaf_rn(sgn, v[i], o);
         }
     }
 }

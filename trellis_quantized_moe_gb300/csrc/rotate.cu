@@ -109,20 +109,154 @@ __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
     }
 }
 
+// Large layers: a warp takes 16 consecutive packed rows of one projection and
+// 8 blocks; each lane streams its 64 bytes of the next rows' activations into
+// a 3-deep per-warp ring in shared memory with cp.async (no registers held
+// for the prefetch, so more warps fit), then rotates exactly as k_rotate.  The
+// rotated row goes out through shared memory so that each store instruction
+// writes 512 contiguous bytes (whole 32-byte sectors) instead of 16 bytes
+// every 64.
+constexpr int kRingRows = 16;      // rows per warp
+constexpr int kRingDepth = 3;      // rows in flight per warp
+constexpr int kRingWarps = 6;      // 48 KB of static shared memory per CTA, 4 CTAs per SM
+
+__global__ void __launch_bounds__(kRingWarps * 32, 4) k_rotate_ring(RotateArgs a)
+{
+    __shared__ __align__(16) uint8_t ring[kRingWarps][kRingDepth + 1][32 * 64];   // + the output row
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = blockIdx.x * blockDim.x + tid; i < a.nzero; i += gridDim.x * blockDim.x)
+        a.zero[i] = 0;
+    if (a.hdr_reset && blockIdx.x == 0 && tid == 0)
+        a.hdr_reset[kHdrError] = 0;
+    if (a.hdr && a.hdr[kHdrError])
+        return;
+    const int nblk = a.width / kHb;
+    const int ngroups = (nblk + kBlocksPerWarp - 1) / kBlocksPerWarp;
+    const long wg = (long)blockIdx.x * kRingWarps + warp;
+    const int grp = (int)(wg % ngroups);
+    const int p = (int)((wg / ngroups) % a.nproj);
+    const int row0 = (int)(wg / ((long)ngroups * a.nproj)) * kRingRows;
+    if (row0 >= a.rows)
+        return;
+    const int nr = min(kRingRows, a.rows - row0);
+    const int blk = grp * kBlocksPerWarp + (lane >> 2);
+    const int c = lane & 3;
+    const bool active = blk < nblk;
+    const int col = (active ? blk : 0) * kHb + kFeat * c;
+    long long tok_l = 0;
+    unsigned long long suh_l = 0;
+    if (lane < nr) {
+        const int row = row0 + lane;
+        if (a.packed) {
+            const int f = a.packed[row];
+            tok_l = f / a.topk;
+            const long long e = a.ids_dtype == EXL3_I64 ? static_cast<const int64_t *>(a.ids)[f]
+                                                        : static_cast<const int32_t *>(a.ids)[f];
+            suh_l = static_cast<unsigned long long>(a.t_suh[e * 3 + p]);
+        } else {
+            tok_l = row;
+            suh_l = reinterpret_cast<unsigned long long>(a.suh);
+        }
+    }
+    // lane l's 64 bytes of slot d, its four 16-byte chunks rotated by l so the
+    // lanes of a shared-memory wavefront hit different banks
+    auto chunk_at = [&](int d, int k) -> uint8_t * {
+        return &ring[warp][d][lane * 64 + (((k + lane) & 3) << 4)];
+    };
+    auto fetch = [&](int i) {
+        if (i < nr) {
+            const long long tok = __shfl_sync(0xffffffffu, tok_l, i);
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                static_cast<const uint16_t *>(a.x) + tok * a.width + col);
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             ::"r"(smem_addr(chunk_at(i % kRingDepth, k))), "l"(src + 16 * k) : "memory");
+        } else {
+            __shfl_sync(0xffffffffu, tok_l, 0);   // keep the warp's shuffles in step
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int i = 0; i < kRingDepth; i++)
+        fetch(i);
+    unsigned long long cur_suh = 0;
+    uint32_t sh[kFeat / 2];
+#pragma unroll 1
+    for (int i = 0; i < nr; i++) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRingDepth - 1) : "memory");
+        const unsigned long long suh = __shfl_sync(0xffffffffu, suh_l, i);
+        if (suh != cur_suh) {                    // warp-uniform
+            const uint2 *q = reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(suh) + col);
+#pragma unroll
+            for (int k = 0; k < kFeat / 4; k++) {
+                const uint2 r = q[k];
+                sh[2 * k] = r.x;
+                sh[2 * k + 1] = r.y;
+            }
+            cur_suh = suh;
+        }
+        float v[kFeat];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(chunk_at(i % kRingDepth, k));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                float2 f;
+                if (a.act_dtype == EXL3_BF16)
+                    f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[h]));
+                else
+                    f = __half22float2(*reinterpret_cast<const __half2 *>(&w[h]));
+                const float2 sf = __half22float2(*reinterpret_cast<const __half2 *>(&sh[4 * k + h]));
+                v[8 * k + 2 * h] = f.x * sf.x;
+                v[8 * k + 2 * h + 1] = f.y * sf.y;
+            }
+        }
+        // the slot's words are in registers (v depends on them): refill it
+        fetch(i + kRingDepth);
+        uint4 out[4];
+        rotate_block32(v, c, out);
+        // lane l's features 32c.. of block l/4 are bytes 64l.. of the warp's
+        // 2 KB output span; written lane-major, read back 16 bytes per lane
+        // at 16l + 512k
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            *reinterpret_cast<uint4 *>(chunk_at(kRingDepth, k)) = out[k];
+        __syncwarp();
+        uint8_t *orow = reinterpret_cast<uint8_t *>(a.out + ((size_t)(row0 + i) * a.nproj + p) * a.width +
+                                                    (size_t)grp * kBlocksPerWarp * kHb);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int off = 16 * lane + 512 * k;               // byte in the span
+            const int src_lane = off >> 6, ch = (off >> 4) & 3;
+            if ((off >> 8) + grp * kBlocksPerWarp < nblk) {    // 256 bytes per block
+                const uint4 val = *reinterpret_cast<const uint4 *>(
+                    &ring[warp][kRingDepth][src_lane * 64 + (((ch + src_lane) & 3) << 4)]);
+                *reinterpret_cast<uint4 *>(orow + off) = val;
+            }
+        }
+        __syncwarp();
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s)
 {
     const long groups = (a.width / kHb + kBlocksPerWarp - 1) / kBlocksPerWarp;
-    // 8 rows per warp once there are enough warps to hide load latency
-    // (measured: 4096-route layers -21% rotate time, 1024 rows +27%)
-    const int rpw = a.rows >= 4096 ? 8 : 1;
-    long warps = (long)((a.rows + rpw - 1) / rpw) * a.nproj * groups;
+    // from 4096 rows: 16 rows per warp with the cp.async ring (enough warps
+    // to hide the load latency; fewer rows take one row per warp)
+    if (a.rows >= 4096) {
+        const long warps = (long)((a.rows + kRingRows - 1) / kRingRows) * a.nproj * groups;
+        const long blocks = (warps + kRingWarps - 1) / kRingWarps;
+        k_rotate_ring<<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    const long warps = (long)a.rows * a.nproj * groups;
     long blocks = (warps + 7) / 8;
     if (blocks < 1)
         blocks = 1;
-    if (rpw == 8)
-        k_rotate<8><<<(unsigned)blocks, 256, 0, s>>>(a);
-    else
-        k_rotate<1><<<(unsigned)blocks, 256, 0, s>>>(a);
+    k_rotate<1><<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

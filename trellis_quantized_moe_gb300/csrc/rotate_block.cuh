@@ -75,11 +75,13 @@ __device__ __forceinline__ void rotate_block32(float v[kRotFeat], int c, uint4 o
     }
 #pragma unroll
     for (int m = 1; m < 4; m <<= 1) {
-        const bool upper = c & m;
+        // upper lane: o - v, lower lane: v + o, as one fma with a +-1 factor
+        // (multiplying by +-1 is exact, so the single rounding is the same)
+        const float sgn = (c & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < kRotFeat; i++) {
             const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = upper ? (o - v[i]) : (v[i] + o);
+            v[i] = __fmaf_rn(sgn, v[i], o);
         }
     }
 #pragma unroll
