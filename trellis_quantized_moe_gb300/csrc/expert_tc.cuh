@@ -33,8 +33,9 @@
 //   warp 18     loads the activation (B) tiles with 2D TMA, two boxes per
 //               stage (lanes 0 and 1), into a byte ring that runs as far
 //               ahead of the MMAs as it has room;
-//   warps 19-22 epilogue: read the finished buffer (tcgen05.ld, one TMEM lane
-//               quarter each), transpose 16 routes at a time through shared
+//   warps 19-26 epilogue: warps 19-22 read the finished buffer (tcgen05.ld,
+//               one TMEM lane quarter each), all eight transpose 16 routes at
+//               a time through shared
 //               memory and run the per-row output rotation: gate/up write
 //               Hb(z)*svh*scale in fp32 (the SwiGLU and the down-input
 //               rotation follow in k_tc_gu_finish), down writes its rotated
@@ -67,8 +68,8 @@ constexpr int kTwRingBytes = 24 * 1024;
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kBWarp = 2 + kDecWarps;     // activation producer
-constexpr int kEpiWarp0 = kBWarp + 1;     // first of four epilogue warps
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarp0 = kBWarp + 1;     // first of eight epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr int kThreads = kDecThreads + 96 + kEpiThreads;
 constexpr int kEpiRows = 16;      // routes per epilogue interval
 constexpr int kZsLd = kHb + 4;
@@ -682,9 +683,9 @@ __device__ __forceinline__ void epi_gu_half_row(const GemmArgs &a, const DownCon
 }
 
 // The epilogue warps' share of one item: buffer `buf` of TMEM -> 16 routes at
-// a time through shared memory -> per-row output rotation.  Warp ew (0..3)
-// reads TMEM lane quarter q = its warp index % 4 and runs routes ew*4..ew*4+3
-// of each interval.  The next interval's tcgen05.ld is in flight while the
+// a time through shared memory -> per-row output rotation.  Warps ew 0..3 read
+// TMEM lane quarter q = their warp index % 4; each of the eight warps runs
+// routes 2ew, 2ew+1 of each interval.  The next interval's tcgen05.ld is in flight while the
 // current one is processed; down items look their staging rows up once per
 // item (a dependent global load per row would stall every interval).
 template <int MODE>
@@ -707,18 +708,22 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
     const float fac = (proj_ref<MODE>(a, it.e, it.p).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
     const uint32_t taddr = tbuf + ((uint32_t)(32 * q) << 16);
     uint32_t v[16];
-    tmem_ld16_issue(taddr, v);
+    const bool loader = ew < 4;                 // one warp per TMEM lane quarter loads
+    if (loader)
+        tmem_ld16_issue(taddr, v);
     for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
-        tmem_ld16_wait(v);
+        if (loader) {
+            tmem_ld16_wait(v);
 #pragma unroll
-        for (int j = 0; j < 16; j++)
-            zs[j * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac;
+            for (int j = 0; j < 16; j++)
+                zs[j * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac;
+        }
         named_barrier(2, kEpiThreads);
-        if (r0 + kEpiRows < it.nrows)
+        if (loader && r0 + kEpiRows < it.nrows)
             tmem_ld16_issue(taddr + r0 + kEpiRows, v);
 #pragma unroll
-        for (int h = 0; h < 4; h++) {
-            const int rr = 4 * ew + h, r = r0 + rr;
+        for (int h = 0; h < kEpiRows / (kEpiThreads / 32); h++) {
+            const int rr = (kEpiRows / (kEpiThreads / 32)) * ew + h, r = r0 + rr;
             if (r < it.nrows) {
                 float z[4];
 #pragma unroll
@@ -968,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             // CTA ends; nothing to wait for here
         }
     } else if (warp >= kEpiWarp0) {
-        // ---------------- epilogue (warps 19..22): finished buffers, in item order
+        // ---------------- epilogue (warps 19..26): finished buffers, in item order
         const int ew = warp - kEpiWarp0, q = warp & 3;   // TMEM lane quarter = warp % 4
         float *zs = reinterpret_cast<float *>(smem + S::off_zs);
         int *rowmap = reinterpret_cast<int *>(smem + S::off_rows);
