@@ -126,17 +126,36 @@ def test_linear_prompt_rows_tcgen05(M, K, cb, act):
     assert_close_linear(y[rows], ref, act, f"linear tcgen05 M={M} K={K} cb={cb}")
 
 
-@pytest.mark.parametrize("M", [4900, 5220])
-def test_linear_more_row_tiles_than_sms(M):
-    # more 256-row items than SMs (4900: 20 row tiles x 8 blocks, ragged last
-    # tile; 5220: a 100-row last tile): CTAs run several items, alternating
-    # between the two TMEM accumulators; every row against the oracle, and the
-    # bytes equal those of a launch with fewer items
+@pytest.mark.parametrize("M", [4900, 5056, 5220])
+def test_linear_two_half_items(M):
+    # 256-row items would need a second wave (on 152 SMs: 20 or 21 row tiles x
+    # 8 blocks), so the launch takes items of 288 rows in two 144-row halves,
+    # one wave: 4900 leaves a 4-row last item (empty second half), 5056 a
+    # 160-row one (a 16-row second half), 5220 a 36-row one.  Every row
+    # against the oracle, and the bytes equal those of a launch of 256-row
+    # items
     lw = LinearWorkload(M=M, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
     dp = X.DeviceProjection(lw.proj)
     y = _linear_gpu(lw, dp)
     ref = O.linear(act_to_f64(lw.x, "bf16"), lw.proj)
-    assert_close_linear(to_f64(y), ref, "bf16", f"linear paired M={M}")
+    assert_close_linear(to_f64(y), ref, "bf16", f"linear two-half items M={M}")
+    few = LinearWorkload(M=1024, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
+    few.x = lw.x[:1024]
+    y_few = _linear_gpu(few, dp).view(torch.int16).cpu().numpy()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy()[:1024], y_few)
+
+
+@pytest.mark.parametrize("M", [10000, 10100])
+def test_linear_more_row_tiles_than_sms(M):
+    # too many rows for one wave of 512-row items (on 152 SMs, 19 row groups x
+    # 8 blocks): 256-row items, CTAs run two or three each, alternating between
+    # the two TMEM accumulators (10100: a 116-row last tile); every row against
+    # the oracle, and the bytes equal those of a launch with fewer items
+    lw = LinearWorkload(M=M, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
+    dp = X.DeviceProjection(lw.proj)
+    y = _linear_gpu(lw, dp)
+    ref = O.linear(act_to_f64(lw.x, "bf16"), lw.proj)
+    assert_close_linear(to_f64(y), ref, "bf16", f"linear multi-item M={M}")
     few = LinearWorkload(M=1024, in_f=256, out_f=1024, K=3, cb=CB_MCG, act="bf16", seed=M)
     few.x = lw.x[:1024]
     y_few = _linear_gpu(few, dp).view(torch.int16).cpu().numpy()

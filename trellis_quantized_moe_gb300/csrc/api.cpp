@@ -3,6 +3,7 @@
 // (except exl3_workspace_error, which is documented to synchronise).
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -114,9 +115,9 @@ EncodeTiledFn encode_tiled()
 }
 
 // fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box {kTcKs,
-// 16 << i} with the 128-byte swizzle of a 128-byte row; rows past the end
-// read as zero.
-bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows)
+// 16 << i} with the 128-byte swizzle of a 128-byte row, plus one of box
+// {kTcKs, half_rows} when half_rows > 0; rows past the end read as zero.
+bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows, int half_rows = 0)
 {
     EncodeTiledFn fn = encode_tiled();
     if (fn == nullptr)
@@ -125,10 +126,17 @@ bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows)
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
-    for (int i = 0; i < kTcMaps; i++) {
-        const cuuint32_t box[2] = {(cuuint32_t)kTcKs, (cuuint32_t)(16 << i)};
-        if (fn(&m.act[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    for (int i = 0; i <= kTcMaps; i++) {
+        // the last map: the two-half linear items' box (half_rows rows), else unused
+        const int box_rows = i < kTcMaps ? 16 << i : half_rows;
+        CUtensorMap *dst = i < kTcMaps ? &m.act[i] : &m.half;
+        if (box_rows == 0) {
+            memset(dst, 0, sizeof(*dst));
+            continue;
+        }
+        const cuuint32_t box[2] = {(cuuint32_t)kTcKs, (cuuint32_t)box_rows};
+        if (fn(dst, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
@@ -466,12 +474,22 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
     if (M > kLinearTcMinRows) {
         // prompt-sized inputs: the tcgen05 kernel, items of up to 256 rows x
         // 128 outputs, the whole contraction per item (M <= 128 keeps the
-        // decode regime, so a row's bytes never depend on M there)
-        TcMaps maps;
-        if (!encode_act_maps(maps, ra.out, p->in_features, M))
-            return EXL3_E_CUDA;
+        // decode regime, so a row's bytes never depend on M there).  When
+        // those items would need a second wave, items of up to 512 rows in
+        // two halves (each decoded weight stage feeds both) fill one wave.
         g.split_host = 0;
-        g.n_items_host = ceil_div(M, tc_rows_per_item()) * L.nb;
+        g.lin_rows = tc_rows_per_item();
+        const int rg_per_wave = sms / L.nb;
+        if (ceil_div(M, g.lin_rows) * L.nb > sms && rg_per_wave > 0) {
+            const int r = (ceil_div(M, rg_per_wave) + 31) / 32 * 32;
+            if (r <= 2 * tc_rows_per_item())
+                g.lin_rows = r;
+        }
+        TcMaps maps;
+        const int half_rows = g.lin_rows > tc_rows_per_item() ? g.lin_rows / 2 : 0;
+        if (!encode_act_maps(maps, ra.out, p->in_features, M, half_rows))
+            return EXL3_E_CUDA;
+        g.n_items_host = ceil_div(M, g.lin_rows) * L.nb;
         const int grid = sms < g.n_items_host ? sms : g.n_items_host;
         return launch_tc_linear(g, maps, grid, stream) == cudaSuccess ? EXL3_OK : EXL3_E_CUDA;
     }

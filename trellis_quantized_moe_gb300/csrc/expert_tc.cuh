@@ -41,6 +41,10 @@
 //               rotation follow in k_tc_gu_finish), down writes its rotated
 //               rows to the fp32 staging (the weighted combine follows in
 //               k_tc_combine), the linear writes its output.
+// Linear launches whose 256-row items would take more than one wave use
+// items of up to 512 rows instead, split into two halves with one
+// accumulator buffer each: every decoded A stage then feeds the MMAs of both
+// halves (half the decode work per row) and the items fit in one wave.
 // Additive layers: each residual stage with a nonzero scale on the item's
 // projection is one more pass of stages that every role walks in the same
 // order, accumulating into the same TMEM columns.
@@ -101,6 +105,7 @@ struct Bars {
 // The activation tensor maps: one per TMA box height RB = 16, 32, ..., 256.
 struct TcMapsDev {
     CUtensorMap act[kTcMaps];
+    CUtensorMap half;          // two-half linear items: box {64, lin_rows / 2}
 };
 
 // Activation geometry of one work item: RB = the item's routes rounded up to
@@ -465,8 +470,8 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
     it.nbk = item % a.nb;
     if (MODE == kModeLinear) {
         it.e = 0;
-        it.row0 = rgi * kNT;
-        it.nrows = min(kNT, a.M - it.row0);
+        it.row0 = rgi * a.lin_rows;
+        it.nrows = min(a.lin_rows, a.M - it.row0);
         return it;
     }
     const int4 r = static_cast<const int4 *>(a.rg)[rgi];
@@ -478,6 +483,39 @@ __device__ __forceinline__ TcItem tc_item(const GemmArgs &a, int item)
 
 template <int MODE>
 __device__ __forceinline__ int proj_index(int p) { return MODE == kModeGateUp ? p : 2; }
+
+// The accumulators of one item: one (up to 256 routes or rows), or, for the
+// linear's items of more than 256 rows, two halves of lin_rows / 2 rows
+// (rows past the item's end leave the second half short or empty).  Half h
+// takes the TMEM buffer of the CTA's sub-item count + h.
+struct Halves {
+    int n, hr;          // halves; rows between their first rows
+    int rows[2];
+};
+
+template <int MODE>
+__device__ __forceinline__ bool tc_two_halves(const GemmArgs &a)
+{
+    return MODE == kModeLinear && a.lin_rows > kNT;
+}
+
+template <int MODE>
+__device__ __forceinline__ Halves item_halves(const GemmArgs &a, const TcItem &it)
+{
+    Halves h;
+    if (tc_two_halves<MODE>(a)) {
+        h.n = 2;
+        h.hr = a.lin_rows / 2;
+        h.rows[0] = min(it.nrows, h.hr);
+        h.rows[1] = it.nrows - h.rows[0];
+    } else {
+        h.n = 1;
+        h.hr = 0;
+        h.rows[0] = it.nrows;
+        h.rows[1] = 0;
+    }
+    return h;
+}
 
 // Projection p of expert e: trellis words, width, codebook (linear: its one
 // projection).
@@ -709,7 +747,7 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
     const uint32_t taddr = tbuf + ((uint32_t)(32 * q) << 16);
     uint32_t v[16];
     const bool loader = ew < 4;                 // one warp per TMEM lane quarter loads
-    if (loader)
+    if (loader && it.nrows > 0)
         tmem_ld16_issue(taddr, v);
     for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
         if (loader) {
@@ -870,17 +908,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             const uint64_t bdesc0 = smem_desc_swz(smem_addr(smem + S::off_b), 1024, 128);
             const uint32_t adlo = (uint32_t)adesc0, adhi = (uint32_t)(adesc0 >> 32);
             const uint32_t bdlo = (uint32_t)bdesc0, bdhi = (uint32_t)(bdesc0 >> 32);
-            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x, nit++) {
+            for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
+                const Halves hv = item_halves<MODE>(a, it);
                 const BGeom bg = b_geom(it.nrows);
                 const uint32_t bsub16 = (uint32_t)(bg.rb * 128) >> 4;   // second box of a stage
-                const uint32_t idesc = instr_desc(max(16, (it.nrows + 15) & ~15));
-                const uint32_t buf = nit & 1, use = nit >> 1;
-                // the epilogue has drained this buffer's previous item
-                if (use > 0 && !wait_bar(&B.tempty[buf], (use - 1) & 1, abort, a.hdr))
+                // the epilogue has drained the buffers' previous items
+                uint32_t dt[2], idesc[2];
+                bool ok = true;
+                for (int h = 0; h < hv.n; h++) {
+                    const uint32_t sub = nit + h, buf = sub & 1, use = sub >> 1;
+                    if (use > 0 && !(ok = wait_bar(&B.tempty[buf], (use - 1) & 1, abort, a.hdr)))
+                        break;
+                    dt[h] = tmem + buf * kNT;
+                    idesc[h] = instr_desc(max(16, (hv.rows[h] + 15) & ~15));
+                }
+                if (!ok)
                     break;
                 fence_after();
-                const uint32_t dt = tmem + buf * kNT;
                 // pass 0 (base) opens the accumulator; residual passes add to it
                 bool first = true;
                 for (int ps = 0; ps < tc_num_passes<MODE>(a) && !*abort; ps++) {
@@ -888,29 +933,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                         continue;
                     for (int s = 0; s < nst; s++, ra.next()) {
                         const int slot = ra.slot;
-                        const int bs = (int)(br.n % kMaxBSlots);
-                        const uint32_t boff = br.place((uint32_t)bg.stage_bytes);
-                        if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr) ||
-                            !wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
+                        if (!wait_bar(&B.full[slot], ra.phase, abort, a.hdr))
                             break;
-                        bphase ^= 1u << bs;
-                        fence_after();
                         // address fields stay below 2^14 (shared memory < 256 KB): 32-bit adds
                         const uint32_t alo = adlo + (uint32_t)(slot * (S::a_bytes >> 4));
-                        const uint32_t blo = bdlo + (boff >> 4);
-                        const uint32_t blo2 = blo + bsub16;
-                        mma_f16_lo(dt, alo, adhi, blo, bdhi, idesc, first ? 0u : 1u);
+                        if (hv.n == 1) {
+                            const int bs = (int)(br.n % kMaxBSlots);
+                            const uint32_t boff = br.place((uint32_t)bg.stage_bytes);
+                            if (!wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr))
+                                break;
+                            bphase ^= 1u << bs;
+                            fence_after();
+                            const uint32_t blo = bdlo + (boff >> 4);
+                            const uint32_t blo2 = blo + bsub16;
+                            mma_f16_lo(dt[0], alo, adhi, blo, bdhi, idesc[0], first ? 0u : 1u);
 #pragma unroll
-                        for (int ks = 1; ks < kKS / 16; ks++)
-                            mma_f16_lo(dt, alo + (uint32_t)(ks * 16), adhi,
-                                       (ks >= kKS / 32 ? blo2 : blo) + (uint32_t)((ks % (kKS / 32)) * 2), bdhi, idesc,
-                                       1u);
+                            for (int ks = 1; ks < kKS / 16; ks++)
+                                mma_f16_lo(dt[0], alo + (uint32_t)(ks * 16), adhi,
+                                           (ks >= kKS / 32 ? blo2 : blo) + (uint32_t)((ks % (kKS / 32)) * 2), bdhi,
+                                           idesc[0], 1u);
+                            mma_commit(&B.bempty[bs]);
+                        } else {
+                            // two entries per stage (inputs 0..63, 64..127), each
+                            // the two halves' boxes; every A sub-tile feeds both
+                            const uint32_t ebytes = (uint32_t)hv.hr * 256u;
+                            bool bok = true;
+                            for (int e = 0; e < 2; e++) {
+                                const int bs = (int)(br.n % kMaxBSlots);
+                                const uint32_t boff = br.place(ebytes);
+                                if (!(bok = wait_bar(&B.bfull[bs], (bphase >> bs) & 1, abort, a.hdr)))
+                                    break;
+                                bphase ^= 1u << bs;
+                                fence_after();
+                                for (int h = 0; h < 2; h++) {
+                                    if (hv.rows[h] == 0)
+                                        continue;
+                                    const uint32_t blo = bdlo + ((boff + (uint32_t)(h * hv.hr * 128)) >> 4);
+#pragma unroll
+                                    for (int j = 0; j < kKS / 32; j++) {
+                                        const int ks = e * (kKS / 32) + j;
+                                        mma_f16_lo(dt[h], alo + (uint32_t)(ks * 16), adhi, blo + (uint32_t)(j * 2),
+                                                   bdhi, idesc[h], (first && ks == 0) ? 0u : 1u);
+                                    }
+                                }
+                                mma_commit(&B.bempty[bs]);
+                            }
+                            if (!bok)
+                                break;
+                        }
                         first = false;
                         mma_commit(&B.empty[slot]);
-                        mma_commit(&B.bempty[bs]);
                     }
                 }
-                mma_commit(&B.tfull[buf]);
+                for (int h = 0; h < hv.n; h++)
+                    mma_commit(&B.tfull[(nit + h) & 1]);
+                nit += hv.n;
             }
         }
     } else if (warp == kBWarp) {
@@ -926,17 +1003,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items && !warp_aborted(abort); item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
+                const Halves hv = item_halves<MODE>(a, it);
                 const BGeom bg = b_geom(it.nrows);
-                const CUtensorMap *map = &maps.act[bg.map];
+                // one entry per stage (its two 64-input boxes), or for a two-half
+                // item two entries per stage (per 64 inputs, both halves' boxes)
+                const CUtensorMap *map = hv.n == 1 ? &maps.act[bg.map] : &maps.half;
+                const int nent = hv.n == 1 ? 1 : 2;
+                const uint32_t ebytes = hv.n == 1 ? (uint32_t)bg.stage_bytes : (uint32_t)hv.hr * 256u;
                 const int x0 = (MODE == kModeGateUp) ? it.p * a.in_f : 0;
                 // the same activation tiles again for every residual pass
                 for (int ps = 0; ok && ps < tc_num_passes<MODE>(a); ps++) {
                     if (pass_alpha<MODE>(a, it.e, it.p, ps) == 0.0f)
                         continue;
-                    for (int s = 0; ok && s < nst; s++) {
+                    for (int se = 0; ok && se < nst * nent; se++) {
+                        const int s = se / nent, en = se % nent;
                         const int bs = (int)(br.n % kMaxBSlots);
-                        const uint32_t o = br.place((uint32_t)bg.stage_bytes);
-                        const uint32_t e = o + (uint32_t)bg.stage_bytes;
+                        const uint32_t o = br.place(ebytes);
+                        const uint32_t e = o + ebytes;
                         // retire the oldest stages until none in flight overlaps [o, e)
                         // and barrier bs is free
                         while (ok) {
@@ -961,11 +1044,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                         }
                         uint8_t *dst = smem + S::off_b + o;
                         if (lane == 0)
-                            mbar_arrive_expect_tx(&B.bfull[bs], bg.stage_bytes);
+                            mbar_arrive_expect_tx(&B.bfull[bs], ebytes);
                         __syncwarp();
-                        if (lane < 2)
-                            tma_load_2d(dst + lane * bg.rb * 128, map, x0 + s * kKS + lane * (kKS / 2), it.row0,
-                                        &B.bfull[bs]);
+                        if (lane < 2) {
+                            if (hv.n == 1)
+                                tma_load_2d(dst + lane * bg.rb * 128, map, x0 + s * kKS + lane * (kKS / 2), it.row0,
+                                            &B.bfull[bs]);
+                            else
+                                tma_load_2d(dst + lane * hv.hr * 128, map, s * kKS + en * (kKS / 2),
+                                            it.row0 + lane * hv.hr, &B.bfull[bs]);
+                        }
                     }
                 }
             }
@@ -979,23 +1067,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         int *rowmap = reinterpret_cast<int *>(smem + S::off_rows);
         volatile int *go = reinterpret_cast<volatile int *>(smem + S::off_misc + 24);
         uint32_t nit = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, nit++) {
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const TcItem it = tc_item<MODE>(a, item);
-            const uint32_t buf = nit & 1, use = nit >> 1;
-            // one thread waits for the buffer; the four warps learn the
-            // outcome together at the named barrier, so all of them take the
-            // same barriers until the end
-            if (ew == 0 && lane == 0)
-                *go = !*abort && wait_bar(&B.tfull[buf], use & 1, abort, a.hdr);
-            named_barrier(2, kEpiThreads);
-            const bool ok = *go != 0;
-            named_barrier(2, kEpiThreads);
-            if (!ok)
-                break;
-            fence_after();
-            tc_item_epilogue<MODE>(a, it, tmem + buf * kNT, zs, rowmap, ew, q);
-            fence_before();
-            warp_arrive(&B.tempty[buf]);
+            const Halves hv = item_halves<MODE>(a, it);
+            for (int h = 0; h < hv.n; h++, nit++) {
+                const uint32_t buf = nit & 1, use = nit >> 1;
+                // one thread waits for the buffer; the eight warps learn the
+                // outcome together at the named barrier, so all of them take
+                // the same barriers until the end
+                if (ew == 0 && lane == 0)
+                    *go = !*abort && wait_bar(&B.tfull[buf], use & 1, abort, a.hdr);
+                named_barrier(2, kEpiThreads);
+                ok = *go != 0;
+                named_barrier(2, kEpiThreads);
+                if (!ok)
+                    break;
+                fence_after();
+                TcItem hi = it;
+                hi.row0 = it.row0 + h * hv.hr;
+                hi.nrows = hv.rows[h];
+                if (hi.nrows > 0)
+                    tc_item_epilogue<MODE>(a, hi, tmem + buf * kNT, zs, rowmap, ew, q);
+                fence_before();
+                warp_arrive(&B.tempty[buf]);
+            }
         }
     } else {
         // ---------------- decode (warps 2..17)
@@ -1036,6 +1132,7 @@ cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStrea
     TcMapsDev m;
     static_assert(sizeof(m.act) == sizeof(maps.act), "tensor map table");
     memcpy(m.act, maps.act, sizeof(m.act));
+    m.half = maps.half;
     k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
     return cudaGetLastError();
 }

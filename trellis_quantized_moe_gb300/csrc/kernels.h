@@ -64,6 +64,9 @@ struct GemmArgs {
     const void *rg;                 // int4 row groups (fused layer)
     // linear: host-planned work
     int M, n_items_host, split_host;
+    // tcgen05 linear: rows per item (256; above that an item is two halves of
+    // lin_rows / 2 rows sharing each decoded weight stage)
+    int lin_rows;
     const uint16_t *act;            // fp16 rows (rotated activations)
     long act_row_stride;            // halves between rows
     // gate/up of small decode-regime layers: rotate the raw activations x
@@ -109,11 +112,13 @@ cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
 // Prefill-regime activation tensor maps: 2D fp16 [rows][cols] views of the
 // rotated activations, one map per box height 16 << i rows; a box {kTcKs,
-// 16 << i} (128-byte rows, 128-byte swizzle) is one stage's B tile.
+// 16 << i} (128-byte rows, 128-byte swizzle) is one stage's B tile.  `half`:
+// the linear's two-half items, box {kTcKs, lin_rows / 2} (unused otherwise).
 constexpr int kTcMaps = 5;
 constexpr int kTcKs = 64;
 struct TcMaps {
     CUtensorMap act[kTcMaps];
+    CUtensorMap half;
 };
 cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
