@@ -250,6 +250,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     ra.x = x;
     ra.act_dtype = act_dtype;
     ra.rows = R;
+    ra.num_sms = sms;
     ra.width = hidden;
     ra.nproj = 2;
     ra.packed = rp.packed;
@@ -442,6 +443,7 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
     ra.x = x;
     ra.act_dtype = act_dtype;
     ra.rows = M;
+    ra.num_sms = sms;
     ra.width = p->in_features;
     ra.nproj = 1;
     ra.suh = p->suh;

@@ -53,6 +53,8 @@ struct RotateArgs {
     int32_t *zero;                  // words to clear
     int nzero;
     int32_t *hdr_reset;             // linear: header to reset (error word)
+    int num_sms;                    // sizes the large-layer grid (rows per warp)
+    int rpw;                        // large layers: rows per warp (set by launch_rotate)
 };
 
 enum GemmMode { kModeGateUp = 0, kModeDown = 1, kModeLinear = 2 };

@@ -109,14 +109,15 @@ __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
     }
 }
 
-// Large layers: a warp takes 16 consecutive packed rows of one projection and
-// 8 blocks; each lane streams its 64 bytes of the next rows' activations into
+// Large layers: a warp takes up to 16 consecutive packed rows (a.rpw, fewer
+// when that would leave SMs short of warps) of one projection and 8 blocks;
+// each lane streams its 64 bytes of the next rows' activations into
 // a 3-deep per-warp ring in shared memory with cp.async (no registers held
 // for the prefetch, so more warps fit), then rotates exactly as k_rotate.  The
 // rotated row goes out through shared memory so that each store instruction
 // writes 512 contiguous bytes (whole 32-byte sectors) instead of 16 bytes
 // every 64.
-constexpr int kRingRows = 16;      // rows per warp
+constexpr int kRingRows = 16;      // rows per warp, at most
 constexpr int kRingDepth = 3;      // rows in flight per warp
 constexpr int kRingWarps = 6;      // 48 KB of static shared memory per CTA, 4 CTAs per SM
 
@@ -135,10 +136,10 @@ __global__ void __launch_bounds__(kRingWarps * 32, 4) k_rotate_ring(RotateArgs a
     const long wg = (long)blockIdx.x * kRingWarps + warp;
     const int grp = (int)(wg % ngroups);
     const int p = (int)((wg / ngroups) % a.nproj);
-    const int row0 = (int)(wg / ((long)ngroups * a.nproj)) * kRingRows;
+    const int row0 = (int)(wg / ((long)ngroups * a.nproj)) * a.rpw;
     if (row0 >= a.rows)
         return;
-    const int nr = min(kRingRows, a.rows - row0);
+    const int nr = min(a.rpw, a.rows - row0);
     const int blk = grp * kBlocksPerWarp + (lane >> 2);
     const int c = lane & 3;
     const bool active = blk < nblk;
@@ -244,12 +245,18 @@ __global__ void __launch_bounds__(kRingWarps * 32, 4) k_rotate_ring(RotateArgs a
 cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s)
 {
     const long groups = (a.width / kHb + kBlocksPerWarp - 1) / kBlocksPerWarp;
-    // from 4096 rows: 16 rows per warp with the cp.async ring (enough warps
-    // to hide the load latency; fewer rows take one row per warp)
+    // from 4096 rows: up to 16 rows per warp with the cp.async ring, as many
+    // as leave one full wave of resident warps (4 CTAs of kRingWarps per SM);
+    // fewer rows take one row per warp
     if (a.rows >= 4096) {
-        const long warps = (long)((a.rows + kRingRows - 1) / kRingRows) * a.nproj * groups;
+        RotateArgs b = a;
+        const long tasks = (long)a.rows * a.nproj * groups;
+        const long slots = (long)(a.num_sms > 0 ? a.num_sms : 1) * 4 * kRingWarps;
+        b.rpw = (int)((tasks + slots - 1) / slots);
+        b.rpw = b.rpw < 1 ? 1 : (b.rpw > kRingRows ? kRingRows : b.rpw);
+        const long warps = (long)((a.rows + b.rpw - 1) / b.rpw) * a.nproj * groups;
         const long blocks = (warps + kRingWarps - 1) / kRingWarps;
-        k_rotate_ring<<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(a);
+        k_rotate_ring<<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(b);
         return cudaGetLastError();
     }
     const long warps = (long)a.rows * a.nproj * groups;
