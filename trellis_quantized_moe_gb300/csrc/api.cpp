@@ -298,6 +298,7 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     // tail (measured: M=1 -5%, 16-route layer -15%; above 64 routes the early
     // down CTAs slow gate/up's tail, a 288-expert layer at M=64 by 21%)
     g.pdl = (!tc_ok && R <= kPdlRoutes) ? 1 : 0;
+    g.tc_pdl = (!fuse_rot && g_prof_events == nullptr) ? 1 : 0;
     g.packed = rp.packed;
     g.part = reinterpret_cast<float *>(w + L.part1);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
@@ -315,6 +316,8 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     prof_mark(3, s);
 
     // down: [R][inter] -> [R][hidden] fp32 staging -> combine into out
+    // (launched in plain stream order: it follows k_tc_gu_finish)
+    g.tc_pdl = 0;
     g.in_f = inter;
     g.out_f = hidden;
     g.nb = L.nb2;
@@ -480,6 +483,7 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
         // those items would need a second wave, items of up to 512 rows in
         // two halves (each decoded weight stage feeds both) fill one wave.
         g.split_host = 0;
+        g.tc_pdl = 1;
         g.lin_rows = tc_rows_per_item();
         const int rg_per_wave = sms / L.nb;
         if (ceil_div(M, g.lin_rows) * L.nb > sms && rg_per_wave > 0) {

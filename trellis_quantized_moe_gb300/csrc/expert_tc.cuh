@@ -1001,6 +1001,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             uint32_t tail = 0;                        // oldest stage in flight
             BRing br;
             bool ok = true;
+            // launched during the rotate kernel's tail (programmatic dependent
+            // launch): the trellis stream, the decode and TMEM setup need
+            // nothing from it, the activations do
+            if (a.tc_pdl)
+                grid_dep_wait();
             for (int item = blockIdx.x; ok && item < n_items && !warp_aborted(abort); item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
                 const Halves hv = item_halves<MODE>(a, it);
@@ -1133,8 +1138,25 @@ cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStrea
     static_assert(sizeof(m.act) == sizeof(maps.act), "tensor map table");
     memcpy(m.act, maps.act, sizeof(m.act));
     m.half = maps.half;
-    k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
-    return cudaGetLastError();
+    if (!a.tc_pdl) {
+        k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
+        return cudaGetLastError();
+    }
+    // right after the rotate kernel: programmatic dependent launch, the
+    // activation producer waits for it (every other role reads only the
+    // weights, the plan the route-pack kernel wrote before the rotate kernel
+    // started, and TMEM)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Smem::total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_expert_tc<MODE>, a, m);
 }
 
 template <int MODE>

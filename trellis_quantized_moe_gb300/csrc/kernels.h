@@ -78,6 +78,10 @@ struct GemmArgs {
     // launch with programmatic dependent launch (decode-regime layers): the
     // kernel waits for its predecessor itself, before reading its outputs
     int pdl;
+    // tcgen05 gate/up and linear: the kernel launched just before is the
+    // rotate kernel (started after the route-pack plan was complete), so only
+    // the activation producer needs to wait for it
+    int tc_pdl;
     // expert tables (fused layer)
     const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
     const int32_t *t_K, *t_cb;
