@@ -362,6 +362,20 @@ def run_ours(args):
                           "kernel_us": [1e3 * float(v) for v in kern.mean(axis=0)]}))
         return
 
+    if args.case == "linear":
+        # the prompt-sized linear (5120 -> 1536, K=3 mcg, bf16) at args.M rows
+        from workloads import CB_MCG, LinearWorkload
+        lw = LinearWorkload(M=args.M, in_f=5120, out_f=1536, K=3, cb=CB_MCG, act="bf16", seed=41)
+        ldp = X.DeviceProjection(lw.proj)
+        lx = torch.from_numpy(lw.x.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        ly = torch.empty((lw.M, 1536), dtype=torch.bfloat16, device=dev)
+        lws = torch.empty(X.exl3_linear_workspace_bytes(lw.M, 5120, 1536), dtype=torch.uint8, device=dev)
+        ms, _, _ = timed(lambda: X.exl3_linear(lx, ldp, ly, lws), args.steps, args.warmup)
+        t = float(np.mean(ms))
+        print(json.dumps({"case": f"linear M={args.M}", "us": 1e3 * t,
+                          "tflops_dense_equiv": 2.0 * args.M * 5120 * 1536 / (t * 1e-3) / 1e12}))
+        return
+
     def layer_case(cfg, name, steps, warmup, M=None):
         """One workload's layer: mean step time without events between the
         kernels, the per-kernel split from a separate profiled run, routed
@@ -605,8 +619,8 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--case", default="all", choices=["all", "decode", "prefill"],
-                    help="decode / prefill: only that layer at --M (profiling target)")
+    ap.add_argument("--case", default="all", choices=["all", "decode", "prefill", "linear"],
+                    help="decode / prefill / linear: only that layer at --M (profiling target)")
     ap.add_argument("--M", type=int, default=1)
     args = ap.parse_args()
     if args.impl == "reference":

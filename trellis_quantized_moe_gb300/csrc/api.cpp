@@ -298,7 +298,6 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     // tail (measured: M=1 -5%, 16-route layer -15%; above 64 routes the early
     // down CTAs slow gate/up's tail, a 288-expert layer at M=64 by 21%)
     g.pdl = (!tc_ok && R <= kPdlRoutes) ? 1 : 0;
-    g.tc_pdl = (!fuse_rot && g_prof_events == nullptr) ? 1 : 0;
     g.packed = rp.packed;
     g.part = reinterpret_cast<float *>(w + L.part1);
     g.cnt_split = reinterpret_cast<int32_t *>(w + L.cnt1);
@@ -316,8 +315,6 @@ int run_moe(const void *x, int act_dtype, int M, int hidden, int inter, int E, i
     prof_mark(3, s);
 
     // down: [R][inter] -> [R][hidden] fp32 staging -> combine into out
-    // (launched in plain stream order: it follows k_tc_gu_finish)
-    g.tc_pdl = 0;
     g.in_f = inter;
     g.out_f = hidden;
     g.nb = L.nb2;
@@ -454,6 +451,7 @@ int exl3_linear(const void *x, int act_dtype, int M, const exl3_proj *p, void *y
     ra.zero = reinterpret_cast<int32_t *>(w + L.cnt);
     ra.nzero = L.split_pairs;
     ra.hdr_reset = hdr;
+    ra.trigger = M > kLinearTcMinRows ? 1 : 0;     // the tcgen05 kernel follows
     if (launch_rotate(ra, stream) != cudaSuccess)
         return EXL3_E_CUDA;
 

@@ -952,6 +952,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                                 mma_f16_lo(dt[0], alo + (uint32_t)(ks * 16), adhi,
                                            (ks >= kKS / 32 ? blo2 : blo) + (uint32_t)((ks % (kKS / 32)) * 2), bdhi,
                                            idesc[0], 1u);
+                            // the A slot first: the decode warps wait for it
+                            mma_commit(&B.empty[slot]);
                             mma_commit(&B.bempty[bs]);
                         } else {
                             // two entries per stage (inputs 0..63, 64..127), each
@@ -976,13 +978,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                                                    bdhi, idesc[h], (first && ks == 0) ? 0u : 1u);
                                     }
                                 }
+                                if (e == 1)
+                                    mma_commit(&B.empty[slot]);
                                 mma_commit(&B.bempty[bs]);
                             }
                             if (!bok)
                                 break;
                         }
                         first = false;
-                        mma_commit(&B.empty[slot]);
                     }
                 }
                 for (int h = 0; h < hv.n; h++)
@@ -1142,10 +1145,9 @@ cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStrea
         k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
         return cudaGetLastError();
     }
-    // right after the rotate kernel: programmatic dependent launch, the
-    // activation producer waits for it (every other role reads only the
-    // weights, the plan the route-pack kernel wrote before the rotate kernel
-    // started, and TMEM)
+    // the linear, right after the rotate kernel: programmatic dependent
+    // launch, the activation producer waits for it (every other role reads
+    // only the weights and TMEM)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

@@ -55,6 +55,10 @@ struct RotateArgs {
     int32_t *hdr_reset;             // linear: header to reset (error word)
     int num_sms;                    // sizes the large-layer grid (rows per warp)
     int rpw;                        // large layers: rows per warp (set by launch_rotate)
+    // let the next kernel (launched with programmatic dependent launch) start
+    // once every CTA of this grid is running: the tcgen05 linear only (early
+    // resident decode-regime CTAs crowd out the rotate's blocks)
+    int trigger;
 };
 
 enum GemmMode { kModeGateUp = 0, kModeDown = 1, kModeLinear = 2 };
@@ -78,9 +82,8 @@ struct GemmArgs {
     // launch with programmatic dependent launch (decode-regime layers): the
     // kernel waits for its predecessor itself, before reading its outputs
     int pdl;
-    // tcgen05 gate/up and linear: the kernel launched just before is the
-    // rotate kernel (started after the route-pack plan was complete), so only
-    // the activation producer needs to wait for it
+    // tcgen05 linear: the kernel launched just before is the rotate kernel,
+    // so only the activation producer needs to wait for it
     int tc_pdl;
     // expert tables (fused layer)
     const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;

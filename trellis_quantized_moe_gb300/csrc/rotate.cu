@@ -15,10 +15,11 @@ template <int RPW>
 __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
 {
     const int tid = threadIdx.x, lane = tid & 31;
-    // a kernel launched after this one with programmatic dependent launch
-    // may start once every CTA of this grid is running (it waits for this
-    // grid's completion before it reads the rotated rows)
-    grid_dep_launch();
+    // the tcgen05 linear, launched after this kernel with programmatic
+    // dependent launch, may start once every CTA of this grid is running (its
+    // activation producer waits for this grid's completion)
+    if (a.trigger)
+        grid_dep_launch();
     for (int i = blockIdx.x * 256 + tid; i < a.nzero; i += gridDim.x * 256)
         a.zero[i] = 0;
     if (a.hdr_reset && blockIdx.x == 0 && tid == 0)
@@ -129,7 +130,8 @@ __global__ void __launch_bounds__(kRingWarps * 32, 4) k_rotate_ring(RotateArgs a
 {
     __shared__ __align__(16) uint8_t ring[kRingWarps][kRingDepth + 1][32 * 64];   // + the output row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    grid_dep_launch();                           // as in k_rotate
+    if (a.trigger)
+        grid_dep_launch();                       // as in k_rotate
     for (int i = blockIdx.x * blockDim.x + tid; i < a.nzero; i += gridDim.x * blockDim.x)
         a.zero[i] = 0;
     if (a.hdr_reset && blockIdx.x == 0 && tid == 0)
