@@ -115,8 +115,8 @@ EncodeTiledFn encode_tiled()
 }
 
 // fp16 [rows][cols] (row pitch cols * 2 bytes) -> one map per box {kTcKs,
-// 16 << i} with the 128-byte swizzle of a 128-byte row, plus one of box
-// {kTcKs, half_rows} when half_rows > 0; rows past the end read as zero.
+// 16 << i} with the 128-byte swizzle of a 128-byte row, or (half_rows > 0)
+// only the map of box {kTcKs, half_rows}; rows past the end read as zero.
 bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows, int half_rows = 0)
 {
     EncodeTiledFn fn = encode_tiled();
@@ -126,14 +126,14 @@ bool encode_act_maps(TcMaps &m, const void *base, int cols, int rows, int half_r
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B;
-    for (int i = 0; i <= kTcMaps; i++) {
-        // the last map: the two-half linear items' box (half_rows rows), else unused
-        const int box_rows = i < kTcMaps ? 16 << i : half_rows;
-        CUtensorMap *dst = i < kTcMaps ? &m.act[i] : &m.half;
-        if (box_rows == 0) {
-            memset(dst, 0, sizeof(*dst));
+    for (int i = 0; i < kTcMaps; i++) {
+        // two-half linear items: only act[0], of box height half_rows
+        if (half_rows > 0 && i > 0) {
+            memset(&m.act[i], 0, sizeof(m.act[i]));
             continue;
         }
+        const int box_rows = half_rows > 0 ? half_rows : 16 << i;
+        CUtensorMap *dst = &m.act[i];
         const cuuint32_t box[2] = {(cuuint32_t)kTcKs, (cuuint32_t)box_rows};
         if (fn(dst, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -102,10 +102,10 @@ struct Bars {
     uint64_t *full, *empty, *twfull, *twempty, *bfull, *bempty, *tfull, *tempty;
 };
 
-// The activation tensor maps: one per TMA box height RB = 16, 32, ..., 256.
+// The activation tensor maps: one per TMA box height RB = 16, 32, ..., 256;
+// a launch of two-half linear items has one, act[0], of box {64, lin_rows / 2}.
 struct TcMapsDev {
     CUtensorMap act[kTcMaps];
-    CUtensorMap half;          // two-half linear items: box {64, lin_rows / 2}
 };
 
 // Activation geometry of one work item: RB = the item's routes rounded up to
@@ -1004,18 +1004,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             uint32_t tail = 0;                        // oldest stage in flight
             BRing br;
             bool ok = true;
-            // launched during the rotate kernel's tail (programmatic dependent
-            // launch): the trellis stream, the decode and TMEM setup need
-            // nothing from it, the activations do
-            if (a.tc_pdl)
-                grid_dep_wait();
+            // the linear, launched during the rotate kernel's tail
+            // (programmatic dependent launch): the trellis stream, the decode
+            // and TMEM setup need nothing from it, the activations do.  Only
+            // the linear's kernel contains the wait (with the dependent-launch
+            // instructions in every instantiation, here and in the rotate
+            // kernels, the additive layer ran 2.5% slower although its kernels
+            // never execute them).
+            if constexpr (MODE == kModeLinear) {
+                if (a.tc_pdl)
+                    grid_dep_wait();
+            }
             for (int item = blockIdx.x; ok && item < n_items && !warp_aborted(abort); item += gridDim.x) {
                 const TcItem it = tc_item<MODE>(a, item);
                 const Halves hv = item_halves<MODE>(a, it);
                 const BGeom bg = b_geom(it.nrows);
                 // one entry per stage (its two 64-input boxes), or for a two-half
                 // item two entries per stage (per 64 inputs, both halves' boxes)
-                const CUtensorMap *map = hv.n == 1 ? &maps.act[bg.map] : &maps.half;
+                const CUtensorMap *map = &maps.act[hv.n == 1 ? bg.map : 0];
                 const int nent = hv.n == 1 ? 1 : 2;
                 const uint32_t ebytes = hv.n == 1 ? (uint32_t)bg.stage_bytes : (uint32_t)hv.hr * 256u;
                 const int x0 = (MODE == kModeGateUp) ? it.p * a.in_f : 0;
@@ -1140,7 +1146,6 @@ cudaError_t launch_tc(const GemmArgs &a, const TcMaps &maps, int grid, cudaStrea
     TcMapsDev m;
     static_assert(sizeof(m.act) == sizeof(maps.act), "tensor map table");
     memcpy(m.act, maps.act, sizeof(m.act));
-    m.half = maps.half;
     if (!a.tc_pdl) {
         k_expert_tc<MODE><<<grid, kThreads, Smem::total, s>>>(a, m);
         return cudaGetLastError();

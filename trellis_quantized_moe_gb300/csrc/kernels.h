@@ -70,9 +70,6 @@ struct GemmArgs {
     const void *rg;                 // int4 row groups (fused layer)
     // linear: host-planned work
     int M, n_items_host, split_host;
-    // tcgen05 linear: rows per item (256; above that an item is two halves of
-    // lin_rows / 2 rows sharing each decoded weight stage)
-    int lin_rows;
     const uint16_t *act;            // fp16 rows (rotated activations)
     long act_row_stride;            // halves between rows
     // gate/up of small decode-regime layers: rotate the raw activations x
@@ -82,9 +79,6 @@ struct GemmArgs {
     // launch with programmatic dependent launch (decode-regime layers): the
     // kernel waits for its predecessor itself, before reading its outputs
     int pdl;
-    // tcgen05 linear: the kernel launched just before is the rotate kernel,
-    // so only the activation producer needs to wait for it
-    int tc_pdl;
     // expert tables (fused layer)
     const int64_t *t_trellis, *t_suh, *t_svh, *t_scale;
     const int32_t *t_K, *t_cb;
@@ -110,6 +104,12 @@ struct GemmArgs {
     int32_t *cnt_comb;
     void *out;                      // down: [M][hidden] act; linear: [M][out] act
     int M_tokens;
+    // tcgen05 linear: rows per item (256; above that an item is two halves of
+    // lin_rows / 2 rows sharing each decoded weight stage)
+    int lin_rows;
+    // tcgen05 linear: the kernel launched just before is the rotate kernel,
+    // so only the activation producer needs to wait for it
+    int tc_pdl;
 };
 
 int route_pack_hist_warps(int E, int R);
@@ -121,13 +121,13 @@ cudaError_t launch_gemm_down(bool additive, int nrb, const GemmArgs &a, int grid
 cudaError_t launch_gemm_linear(const GemmArgs &a, int grid, cudaStream_t s);
 // Prefill-regime activation tensor maps: 2D fp16 [rows][cols] views of the
 // rotated activations, one map per box height 16 << i rows; a box {kTcKs,
-// 16 << i} (128-byte rows, 128-byte swizzle) is one stage's B tile.  `half`:
-// the linear's two-half items, box {kTcKs, lin_rows / 2} (unused otherwise).
+// 16 << i} (128-byte rows, 128-byte swizzle) is one stage's B tile.  A
+// launch of the linear's two-half items uses only act[0], of box {kTcKs,
+// lin_rows / 2}.
 constexpr int kTcMaps = 5;
 constexpr int kTcKs = 64;
 struct TcMaps {
     CUtensorMap act[kTcMaps];
-    CUtensorMap half;
 };
 cudaError_t launch_tc_gateup(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);
 cudaError_t launch_tc_down(const GemmArgs &a, const TcMaps &maps, int grid, cudaStream_t s);

@@ -11,14 +11,15 @@ namespace exl3 {
 constexpr int kBlocksPerWarp = 8;
 constexpr int kFeat = kRotFeat;
 
-template <int RPW>
+// TRIGGER: the tcgen05 linear, launched after this kernel with programmatic
+// dependent launch, may start once every CTA of this grid is running (its
+// activation producer waits for this grid's completion).  A separate
+// instantiation: the fused layer's rotate kernels do not contain the trigger.
+template <int RPW, bool TRIGGER>
 __global__ void __launch_bounds__(256) k_rotate(RotateArgs a)
 {
     const int tid = threadIdx.x, lane = tid & 31;
-    // the tcgen05 linear, launched after this kernel with programmatic
-    // dependent launch, may start once every CTA of this grid is running (its
-    // activation producer waits for this grid's completion)
-    if (a.trigger)
+    if constexpr (TRIGGER)
         grid_dep_launch();
     for (int i = blockIdx.x * 256 + tid; i < a.nzero; i += gridDim.x * 256)
         a.zero[i] = 0;
@@ -126,11 +127,12 @@ constexpr int kRingRows = 16;      // rows per warp, at most
 constexpr int kRingDepth = 3;      // rows in flight per warp
 constexpr int kRingWarps = 6;      // 48 KB of static shared memory per CTA, 4 CTAs per SM
 
+template <bool TRIGGER>
 __global__ void __launch_bounds__(kRingWarps * 32, 4) k_rotate_ring(RotateArgs a)
 {
     __shared__ __align__(16) uint8_t ring[kRingWarps][kRingDepth + 1][32 * 64];   // + the output row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (a.trigger)
+    if constexpr (TRIGGER)
         grid_dep_launch();                       // as in k_rotate
     for (int i = blockIdx.x * blockDim.x + tid; i < a.nzero; i += gridDim.x * blockDim.x)
         a.zero[i] = 0;
@@ -263,14 +265,20 @@ cudaError_t launch_rotate(const RotateArgs &a, cudaStream_t s)
         b.rpw = b.rpw < 1 ? 1 : (b.rpw > kRingRows ? kRingRows : b.rpw);
         const long warps = (long)((a.rows + b.rpw - 1) / b.rpw) * a.nproj * groups;
         const long blocks = (warps + kRingWarps - 1) / kRingWarps;
-        k_rotate_ring<<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(b);
+        if (a.trigger)
+            k_rotate_ring<true><<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(b);
+        else
+            k_rotate_ring<false><<<(unsigned)blocks, kRingWarps * 32, 0, s>>>(b);
         return cudaGetLastError();
     }
     const long warps = (long)a.rows * a.nproj * groups;
     long blocks = (warps + 7) / 8;
     if (blocks < 1)
         blocks = 1;
-    k_rotate<1><<<(unsigned)blocks, 256, 0, s>>>(a);
+    if (a.trigger)
+        k_rotate<1, true><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else
+        k_rotate<1, false><<<(unsigned)blocks, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 
