@@ -12,6 +12,7 @@ prompt-sized linear, an end-to-end figure through the C ABI with host buffers
 and the float64 CPU oracle timed on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --case decode|prefill|linear --M ROWS   # one layer (profiling target)
 
 With --gpus N > 1 (under torchrun) every rank runs an independent replica
 (the layer has no exchange step on one GPU); value = tokens of all ranks /
