@@ -517,6 +517,15 @@ __device__ __forceinline__ Halves item_halves(const GemmArgs &a, const TcItem &i
     return h;
 }
 
+// Rows of half 0 of a CTA's last two-half item that the eight epilogue warps
+// drain; the sixteen decode warps take the rest of half 0 and all of half 1
+// (about 40% and 60% of the rows: sixteen warps drain a 16-row interval in
+// about two thirds of the eight epilogue warps' time).  A multiple of 16.
+__device__ __forceinline__ int shared_split(const Halves &hv)
+{
+    return min(hv.rows[0], ((hv.rows[0] + hv.rows[1]) * 2 / 5 + 15) & ~15);
+}
+
 // Projection p of expert e: trellis words, width, codebook (linear: its one
 // projection).
 struct ProjRef {
@@ -720,16 +729,19 @@ __device__ __forceinline__ void epi_gu_half_row(const GemmArgs &a, const DownCon
         make_float4(z[0], z[1], z[2], z[3]);
 }
 
-// The epilogue warps' share of one item: buffer `buf` of TMEM -> 16 routes at
-// a time through shared memory -> per-row output rotation.  Warps ew 0..3 read
-// TMEM lane quarter q = their warp index % 4; each of the eight warps runs
-// routes 2ew, 2ew+1 of each interval.  The next interval's tcgen05.ld is in flight while the
-// current one is processed; down items look their staging rows up once per
-// item (a dependent global load per row would stall every interval).
-template <int MODE>
+// A team of NW warps' share of one item: rows [r_begin, it.nrows) of buffer
+// `buf` of TMEM -> 16 routes at a time through shared memory -> per-row
+// output rotation.  Warps ew 0..3 read TMEM lane quarter q = their warp index
+// % 4; each warp runs 16/NW routes of each interval.  The next interval's
+// tcgen05.ld is in flight while the current one is processed; down items look
+// their staging rows up once per item (a dependent global load per row would
+// stall every interval).  The team meets at named barrier `bar`.
+template <int MODE, int NW>
 __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem &it, uint32_t tbuf, float *zs,
-                                                 int *rowmap, int ew, int q)
+                                                 int *rowmap, int ew, int q, int r_begin, int bar)
 {
+    constexpr int kRpw = kEpiRows / NW;         // routes per warp and interval
+    static_assert(kRpw * NW == kEpiRows, "epilogue team size");
     const int lane = threadIdx.x & 31;
     DownConsts cd;
     const int pi = proj_index<MODE>(it.p);
@@ -741,27 +753,27 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
         load_half4(reinterpret_cast<const uint16_t *>(a.t_scale[it.e * 3 + pi]), col, cd.sc);
     }
     if (MODE == kModeDown)
-        for (int r = ew * 32 + lane; r < it.nrows; r += kEpiThreads)
+        for (int r = ew * 32 + lane; r < it.nrows; r += NW * 32)
             rowmap[r] = a.packed[it.row0 + r];
     const float fac = (proj_ref<MODE>(a, it.e, it.p).cb == EXL3_CB_MUL1) ? kInvSqrtMul1 : 1.0f;
     const uint32_t taddr = tbuf + ((uint32_t)(32 * q) << 16);
     uint32_t v[16];
     const bool loader = ew < 4;                 // one warp per TMEM lane quarter loads
-    if (loader && it.nrows > 0)
-        tmem_ld16_issue(taddr, v);
-    for (int r0 = 0; r0 < it.nrows; r0 += kEpiRows) {
+    if (loader && r_begin < it.nrows)
+        tmem_ld16_issue(taddr + r_begin, v);
+    for (int r0 = r_begin; r0 < it.nrows; r0 += kEpiRows) {
         if (loader) {
             tmem_ld16_wait(v);
 #pragma unroll
             for (int j = 0; j < 16; j++)
                 zs[j * kZsLd + 32 * q + lane] = __uint_as_float(v[j]) * fac;
         }
-        named_barrier(2, kEpiThreads);
+        named_barrier(bar, NW * 32);
         if (loader && r0 + kEpiRows < it.nrows)
             tmem_ld16_issue(taddr + r0 + kEpiRows, v);
 #pragma unroll
-        for (int h = 0; h < kEpiRows / (kEpiThreads / 32); h++) {
-            const int rr = (kEpiRows / (kEpiThreads / 32)) * ew + h, r = r0 + rr;
+        for (int h = 0; h < kRpw; h++) {
+            const int rr = kRpw * ew + h, r = r0 + rr;
             if (r < it.nrows) {
                 float z[4];
 #pragma unroll
@@ -781,7 +793,7 @@ __device__ __forceinline__ void tc_item_epilogue(const GemmArgs &a, const TcItem
                 }
             }
         }
-        named_barrier(2, kEpiThreads);
+        named_barrier(bar, NW * 32);
     }
 }
 
@@ -1085,8 +1097,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const TcItem it = tc_item<MODE>(a, item);
             const Halves hv = item_halves<MODE>(a, it);
+            // the CTA's last two-half item: the decode warps, idle by then,
+            // take the tail of half 0 and all of half 1
+            const bool shared = tc_two_halves<MODE>(a) && item + (int)gridDim.x >= n_items;
             for (int h = 0; h < hv.n; h++, nit++) {
                 const uint32_t buf = nit & 1, use = nit >> 1;
+                if (shared && h == 1)
+                    break;
                 // one thread waits for the buffer; the eight warps learn the
                 // outcome together at the named barrier, so all of them take
                 // the same barriers until the end
@@ -1100,9 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
                 fence_after();
                 TcItem hi = it;
                 hi.row0 = it.row0 + h * hv.hr;
-                hi.nrows = hv.rows[h];
+                hi.nrows = shared ? shared_split(hv) : hv.rows[h];
                 if (hi.nrows > 0)
-                    tc_item_epilogue<MODE>(a, hi, tmem + buf * kNT, zs, rowmap, ew, q);
+                    tc_item_epilogue<MODE, kEpiThreads / 32>(a, hi, tmem + buf * kNT, zs, rowmap, ew, q, 0, 2);
                 fence_before();
                 warp_arrive(&B.tempty[buf]);
             }
@@ -1119,6 +1136,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_expert_tc(GemmArgs a, const __g
             const TcItem it = tc_item<MODE>(a, item);
             if (!tc_item_decode<MODE>(a, smem, B, abort, it, ra, rt, tg, t, m))
                 break;
+        }
+        if constexpr (MODE == kModeLinear) {
+            // the CTA's last two-half item: rows [split, rows0) of half 0 and
+            // all of half 1, as a team of 16 warps (named barrier 3)
+            // transposing through the A ring, free once the item's MMAs have
+            // completed.  Every decode warp takes this path (the item is fixed
+            // by the launch, not by how far the loop above got), so the team's
+            // barriers always fill; after a timeout the go flag ends it.
+            const int last = (int)blockIdx.x + (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x * (int)gridDim.x;
+            if (tc_two_halves<MODE>(a)) {
+                const TcItem it = tc_item<MODE>(a, last);
+                const Halves hv = item_halves<MODE>(a, it);
+                const int split = shared_split(hv);
+                const uint32_t use = (uint32_t)((last - (int)blockIdx.x) / (int)gridDim.x);   // items before it
+                const int ew = warp - 2, q = warp & 3;
+                float *zs = reinterpret_cast<float *>(smem + S::off_a);
+                volatile int *go = reinterpret_cast<volatile int *>(smem + S::off_misc + 32);
+                for (int h = 0; h < 2; h++) {
+                    const int r_begin = h == 0 ? split : 0;
+                    if (r_begin >= hv.rows[h])
+                        continue;
+                    // its sub-items are 2*use (buffer 0) and 2*use + 1 (buffer 1)
+                    if (ew == 0 && lane == 0)
+                        *go = !*abort && wait_bar(&B.tfull[h], use & 1, abort, a.hdr);
+                    named_barrier(3, kDecThreads);
+                    const bool go_on = *go != 0;
+                    named_barrier(3, kDecThreads);
+                    if (!go_on)
+                        break;
+                    fence_after();
+                    TcItem hi = it;
+                    hi.row0 = it.row0 + h * hv.hr;
+                    hi.nrows = hv.rows[h];
+                    tc_item_epilogue<MODE, kDecWarps>(a, hi, tmem + (uint32_t)h * kNT, zs, nullptr, ew, q, r_begin, 3);
+                    fence_before();
+                }
+            }
         }
     }
 
