@@ -76,6 +76,37 @@ def test_single_route_unit_weight_is_the_expert_chain():
         assert np.allclose(out[t], d[0], rtol=1e-12, atol=1e-14)
 
 
+def _with_scale_times(proj, factor):
+    # a copy whose per-channel output scale is multiplied by an exact power of
+    # two (so the fp16 scale stays exact): the projection's output times factor
+    from dataclasses import replace
+    return replace(proj, scale=(proj.scale.astype(np.float64) * factor).astype(np.float16))
+
+
+def test_swiglu_gates_through_the_gate_projection():
+    # SwiGLU = silu(gate) * up: the expert's output is linear in the up
+    # projection, and SiLU's odd part is the identity (silu(g) - silu(-g) = g
+    # because sigma(g) + sigma(-g) = 1), so negating the gate projection moves
+    # the output by exactly down(gate(x) * up(x)).  A nonlinearity on the up
+    # branch fails the first check; a missing one fails the second.
+    get = _experts()
+    x = np.random.default_rng(11).standard_normal((3, H))
+    ids = np.array([[1], [3], [0]])
+    rw = np.ones((3, 1))
+    base = O.moe_forward(x, ids, rw, get)
+    up2 = O.moe_forward(x, ids, rw, lambda e, p: _with_scale_times(get(e, p), -2.0) if p == 1 else get(e, p))
+    assert np.allclose(up2, -2.0 * base, rtol=1e-11, atol=1e-12 * np.abs(base).max())
+    neg = O.moe_forward(x, ids, rw, lambda e, p: _with_scale_times(get(e, p), -1.0) if p == 0 else get(e, p))
+    for t in range(3):
+        e = ids[t, 0]
+        g = O.linear(x[t:t + 1], get(e, 0))
+        u = O.linear(x[t:t + 1], get(e, 1))
+        want = O.linear(g * u, get(e, 2))[0]
+        assert np.allclose(base[t] - neg[t], want, rtol=1e-9, atol=1e-11 * np.abs(want).max())
+        # and the gate side is not linear: negating it is not negating the output
+        assert np.abs(neg[t] + base[t]).max() > 1e-3 * np.abs(base[t]).max()
+
+
 def test_combine_is_linear_in_route_weights_and_counts_duplicates():
     get = _experts()
     x = np.random.default_rng(2).standard_normal((4, H))
